@@ -1,0 +1,202 @@
+/*
+ * pvl.h — packed variable-length masked attention for GB300 (sm_103a).
+ *
+ * C ABI of libpvl.so.  Several variable-length episodes share one [B, L]
+ * token grid, either zero-padded to a common frame count (one episode per
+ * batch row) or concatenated along the sequence axis; every token carries a
+ * seq_id, and query i may attend key j iff seq_id[i] == seq_id[j] >= 0.
+ * Sources: "lingbot_va_packing" §2.1 (pad-collate, valid_frames, seq_id -1
+ * for padding frames in FlexAttnFunc.init_mask), "furniture_packing_variable_
+ * length" (seq_id -1 keeps padding out of attention on the query and key side
+ * and blocks leaks between episodes), "lingbot_va_attn_profiling" (packing
+ * proposal: per-token document id and the mask condition doc_id[q] ==
+ * doc_id[k]).
+ *
+ * Conventions for every call:
+ *  - Tensors are dense and contiguous.  Q, K, V, O, dO, dQ, dK, dV are bf16
+ *    [B, L, H, D] (D fastest).  LSE is fp32 [B, H, L].  seq_id is int32 [B, L].
+ *  - Pointers marked "dev" are device pointers of the current CUDA device;
+ *    "host" pointers are ordinary host memory read before the call returns.
+ *  - The caller owns and allocates every buffer and the stream.  The library
+ *    allocates no device memory (its only device globals are a 16-byte error
+ *    record per device).  Calls are asynchronous on `stream` (NULL = legacy
+ *    default stream) and return after enqueueing.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    failed check returns a status and launches nothing.  Device-side
+ *    failures (a bounded wait that ran out, a tile map built for another
+ *    shape) are recorded in the device error record and surface through
+ *    pvl_device_error().  No kernel traps or spins without bound.
+ *  - pvl_last_error_message() describes the most recent non-OK status of the
+ *    calling thread.
+ */
+#ifndef PVL_H_
+#define PVL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PVL_API __attribute__((visibility("default")))
+#else
+#define PVL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pvl_status {
+  PVL_OK = 0,
+  PVL_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent table, short workspace */
+  PVL_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement (D, alignment, limits) */
+  PVL_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
+  PVL_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out (reported by pvl_device_error) */
+} pvl_status;
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* pvl_stream_t;
+
+/* Raw bfloat16 bits. */
+typedef uint16_t pvl_bf16;
+
+/* Limits (UNSUPPORTED beyond them). */
+#define PVL_MAX_SEGMENTS 2048     /* B * K of pack_build_seq_ids */
+#define PVL_MAX_L (1 << 19)       /* sequence length */
+#define PVL_MAX_ORDER_TILES 16384 /* B * ceil(L / block) of tile_map_build */
+
+/* ------------------------------------------------------------------------
+ * pack_build_seq_ids — per-token episode id from a segment table.
+ * Defines: "lingbot_va_packing" §2.1 (seq_id of frames >= valid_frames[b]
+ * becomes -1) and "lingbot_va_attn_profiling" (per-token document id of
+ * concatenated episodes).
+ *
+ * seg_frames, seg_valid: host int32 [B * K], row-major [B][K].  Row b holds K
+ *   segments laid end to end; segment k spans seg_frames[b,k] frames of
+ *   tokens_per_frame tokens, of which the first seg_valid[b,k] frames are real.
+ * seq_id: dev int32 [B * L], written completely: id b*K + k on the real
+ *   frames of segment k, -1 on padding frames and past the last segment.
+ * Errors: INVALID_ARG for null pointers, B/K/L/tokens_per_frame < 1, any
+ *   negative entry, seg_valid > seg_frames, or a row needing more than L
+ *   tokens; UNSUPPORTED for B*K > PVL_MAX_SEGMENTS or L > PVL_MAX_L.
+ * ---------------------------------------------------------------------- */
+PVL_API pvl_status pack_build_seq_ids(const int32_t* seg_frames, const int32_t* seg_valid, int B, int K,
+                              int tokens_per_frame, int L, int32_t* seq_id, pvl_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Tile map — which (query tile, key tile) pairs can hold an admissible pair.
+ * Defines: "lingbot_va_packing" §2.1-§2.2 (FlexAttention block mask built from
+ * the seq_ids; the same mask must be seen by forward and backward, so here it
+ * is an explicit argument of both instead of hidden state).
+ *
+ * Rule.  A position p < L with seq_id >= 0 is valid.  Per tile: nv = number
+ * of valid positions, lo/hi = min/max id over them.  A pair is EMPTY (0) if
+ * either nv is 0 or the id ranges do not overlap, FULL (2) if both tiles are
+ * wholly valid and carry one and the same id, PARTIAL (1) otherwise.  EMPTY
+ * pairs hold no admissible pair; FULL pairs hold only admissible pairs.
+ *
+ * Workspace (dev, caller-allocated, tile_map_ws_bytes() bytes, 256-byte
+ * aligned) holds, at the byte offsets tile_map_layout() returns:
+ *   HEADER      int32[16]  magic, version, B, L, block_m, block_n, nTq, nTk
+ *   Q_NV/LO/HI  int32[B*nTq]      K_NV/LO/HI int32[B*nTk]
+ *   CLS         uint8[B*nTq*nTk]  class of (b, qt, kt)
+ *   ROW_COUNT   int32[B*nTq]  non-empty key tiles per query tile
+ *   ROW_FULL    int32[B*nTq]  how many of them are FULL
+ *   ROW_LIST    int32[B*nTq*nTk]  their indices: FULL first, then PARTIAL,
+ *                              each ascending; unused slots -1
+ *   COL_COUNT/COL_FULL int32[B*nTk], COL_LIST int32[B*nTk*nTq]: the same per
+ *                              key tile over query tiles
+ *   Q_ORDER     int32[B*nTq]  b*nTq+qt sorted by descending ROW_COUNT, ties
+ *                              by ascending index (longest work first)
+ *   K_ORDER     int32[B*nTk]  the same over key tiles by COL_COUNT
+ * nTq = ceil(L / block_m), nTk = ceil(L / block_n).
+ * ---------------------------------------------------------------------- */
+enum {
+  PVL_TM_HEADER = 0,
+  PVL_TM_Q_NV, PVL_TM_Q_LO, PVL_TM_Q_HI,
+  PVL_TM_K_NV, PVL_TM_K_LO, PVL_TM_K_HI,
+  PVL_TM_CLS,
+  PVL_TM_ROW_COUNT, PVL_TM_ROW_FULL, PVL_TM_ROW_LIST,
+  PVL_TM_COL_COUNT, PVL_TM_COL_FULL, PVL_TM_COL_LIST,
+  PVL_TM_Q_ORDER, PVL_TM_K_ORDER,
+  PVL_TM_NFIELDS
+};
+
+/* Bytes of workspace for tile_map_build; 0 if the arguments are invalid. */
+PVL_API size_t tile_map_ws_bytes(int B, int L, int block_m, int block_n);
+
+/* Byte offsets of the PVL_TM_NFIELDS arrays inside the workspace (host call,
+ * no device work).  offsets: host size_t[PVL_TM_NFIELDS]. */
+PVL_API pvl_status tile_map_layout(int B, int L, int block_m, int block_n, size_t* offsets);
+
+/* seq_id: dev int32 [B * L].  block_m, block_n in 1..1024 (the attention
+ * calls need 128 and 128).  tile_ws: dev, ws_bytes >= tile_map_ws_bytes().
+ * Errors: INVALID_ARG for null pointers, sizes < 1, a short or misaligned
+ * workspace; UNSUPPORTED for L > PVL_MAX_L or B*nT > PVL_MAX_ORDER_TILES. */
+PVL_API pvl_status tile_map_build(const int32_t* seq_id, int B, int L, int block_m, int block_n, void* tile_ws,
+                          size_t ws_bytes, pvl_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * masked_attn_fwd — O = softmax(scale * Q K^T restricted to admissible keys) V.
+ * Defines: "furniture_packing_variable_length" (attention masking by seq_id)
+ * and "lingbot_va_attn_profiling" (FlexAttention forward, doc_id mask).
+ *
+ * q, k, v: dev bf16 [B, L, H, D], 16-byte aligned.  seq_id: dev int32 [B, L].
+ * tile_ws: a tile map built from this seq_id with block_m = block_n = 128.
+ * D in {64, 128}; H >= 1; scale > 0 (1/sqrt(D) is the usual choice).
+ * o: dev bf16 [B, L, H, D].  lse: dev fp32 [B, H, L], natural-log
+ *   log-sum-exp of the admissible scaled scores.
+ * Rows with no admissible key (seq_id -1) get O = 0 exactly and LSE = -inf.
+ * Errors: INVALID_ARG for null pointers or sizes < 1; UNSUPPORTED for other
+ *   D, misaligned pointers or L > PVL_MAX_L; CUDA for launch failures.  A
+ *   tile map of another shape is detected on the device (INVALID_ARG from
+ *   pvl_device_error, outputs untouched).
+ * ---------------------------------------------------------------------- */
+PVL_API pvl_status masked_attn_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, const int32_t* seq_id,
+                           const void* tile_ws, int B, int L, int H, int D, float scale, pvl_bf16* o,
+                           float* lse, pvl_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * masked_attn_bwd — gradients of the masked attention from the saved LSE.
+ * Defines: the backward of the FlexAttention template the pages run
+ * ("lingbot_va_attn_profiling", kernel table); P is recomputed from LSE and
+ * the score matrix is never stored.
+ *   Delta_i = <dO_i, O_i>,  dS = P * (dO V^T - Delta),
+ *   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+ *
+ * q, k, v, o, dO: dev bf16 [B, L, H, D] (o as written by masked_attn_fwd);
+ * lse: dev fp32 [B, H, L] from masked_attn_fwd; seq_id, tile_ws as for the
+ * forward.  dq, dk, dv: dev bf16 [B, L, H, D], fully written; rows with
+ * seq_id -1 get exact zeros.
+ * ws: dev scratch of masked_attn_bwd_ws_bytes(B, L, H, D) bytes, 256-byte
+ *   aligned (fp32 dQ accumulator and Delta); contents on entry are ignored.
+ * Errors: as masked_attn_fwd, plus INVALID_ARG for a short workspace.
+ * ---------------------------------------------------------------------- */
+PVL_API size_t masked_attn_bwd_ws_bytes(int B, int L, int H, int D);
+
+PVL_API pvl_status masked_attn_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, const pvl_bf16* o,
+                           const pvl_bf16* dO, const float* lse, const int32_t* seq_id, const void* tile_ws,
+                           int B, int L, int H, int D, float scale, pvl_bf16* dq, pvl_bf16* dk, pvl_bf16* dv,
+                           void* ws, size_t ws_bytes, pvl_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Device error record.  Synchronises `stream`, reads and clears the current
+ * device's error record.  Returns PVL_OK, PVL_ERR_TIMEOUT (a bounded wait ran
+ * out; the kernel released its resources and returned), PVL_ERR_INVALID_ARG
+ * (tile map of another shape) or PVL_ERR_CUDA (the synchronisation failed).
+ * info (optional, host int32[4]): code, where, block, thread of the first
+ * failure.
+ * ---------------------------------------------------------------------- */
+PVL_API pvl_status pvl_device_error(pvl_stream_t stream);
+PVL_API pvl_status pvl_device_error_detail(pvl_stream_t stream, int32_t* info);
+
+/* Human-readable text of the calling thread's last non-OK status. */
+PVL_API const char* pvl_last_error_message(void);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+PVL_API int pvl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PVL_H_ */

@@ -1,0 +1,215 @@
+"""Python binding of libpvl: argument marshalling only.
+
+Every function checks shapes/dtypes, allocates outputs with torch on the
+tensors' CUDA device when the caller passes none, and calls the C entry point
+of the same name on the current torch stream.  All arithmetic runs in the
+library's CUDA kernels; nothing here computes attention, seq_ids or tile maps.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import _lib
+
+PVL_OK, PVL_ERR_INVALID_ARG, PVL_ERR_UNSUPPORTED, PVL_ERR_CUDA, PVL_ERR_TIMEOUT = range(5)
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT"}
+
+TM_FIELDS = ["header", "q_nv", "q_lo", "q_hi", "k_nv", "k_lo", "k_hi", "cls", "row_count", "row_full",
+             "row_list", "col_count", "col_full", "col_list", "q_order", "k_order"]
+EMPTY, PARTIAL, FULL = 0, 1, 2
+
+
+class PvlError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"pvl {STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def _check(status: int) -> None:
+    if status != PVL_OK:
+        raise PvlError(status, _lib.load().pvl_last_error_message().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+# ------------------------------------------------------------------ seq_ids
+def pack_build_seq_ids(seg_frames, seg_valid, tokens_per_frame: int, L: int, out: torch.Tensor | None = None,
+                       device=None, stream=None) -> torch.Tensor:
+    """int32 [B, L] seq_id on the GPU from host [B, K] frame / valid-frame tables."""
+    frames = np.ascontiguousarray(np.asarray(seg_frames, dtype=np.int32))
+    valid = np.ascontiguousarray(np.asarray(seg_valid, dtype=np.int32))
+    if frames.ndim != 2 or frames.shape != valid.shape:
+        raise ValueError("seg_frames and seg_valid must both be [B, K]")
+    B, K = frames.shape
+    if out is None:
+        out = torch.empty((B, L), dtype=torch.int32, device=device or "cuda")
+    _need_cuda(out, "out", torch.int32, (B, L))
+    with torch.cuda.device(out.device):
+        _check(_lib.load().pack_build_seq_ids(frames.ctypes.data, valid.ctypes.data, B, K, int(tokens_per_frame),
+                                              int(L), out.data_ptr(), _stream(stream)))
+    return out
+
+
+# ----------------------------------------------------------------- tile map
+@dataclass
+class TileMap:
+    """Device workspace written by tile_map_build plus typed views of its arrays."""
+    ws: torch.Tensor
+    B: int
+    L: int
+    block_m: int
+    block_n: int
+    offsets: tuple
+
+    @property
+    def nTq(self) -> int:
+        return -(-self.L // self.block_m)
+
+    @property
+    def nTk(self) -> int:
+        return -(-self.L // self.block_n)
+
+    def field(self, name: str) -> torch.Tensor:
+        i = TM_FIELDS.index(name)
+        B, nq, nk = self.B, self.nTq, self.nTk
+        shapes = {"header": (16,), "q_nv": (B, nq), "q_lo": (B, nq), "q_hi": (B, nq), "k_nv": (B, nk),
+                  "k_lo": (B, nk), "k_hi": (B, nk), "cls": (B, nq, nk), "row_count": (B, nq),
+                  "row_full": (B, nq), "row_list": (B, nq, nk), "col_count": (B, nk), "col_full": (B, nk),
+                  "col_list": (B, nk, nq), "q_order": (B * nq,), "k_order": (B * nk,)}
+        shape = shapes[name]
+        n = int(np.prod(shape))
+        off = self.offsets[i]
+        if name == "cls":
+            return self.ws[off:off + n].view(shape)
+        return self.ws[off:off + 4 * n].view(torch.int32).view(shape)
+
+    def to_host(self) -> dict:
+        out = {name: self.field(name).cpu().numpy() for name in TM_FIELDS}
+        out.update(B=self.B, L=self.L, block_m=self.block_m, block_n=self.block_n, nTq=self.nTq, nTk=self.nTk)
+        return out
+
+
+def tile_map_ws_bytes(B: int, L: int, block_m: int = 128, block_n: int = 128) -> int:
+    return int(_lib.load().tile_map_ws_bytes(B, L, block_m, block_n))
+
+
+def tile_map_build(seq_id: torch.Tensor, block_m: int = 128, block_n: int = 128,
+                   ws: torch.Tensor | None = None, stream=None) -> TileMap:
+    lib = _lib.load()
+    if seq_id.dim() != 2:
+        raise ValueError("seq_id must be [B, L]")
+    _need_cuda(seq_id, "seq_id", torch.int32)
+    B, L = seq_id.shape
+    nbytes = int(lib.tile_map_ws_bytes(B, L, block_m, block_n))
+    if nbytes == 0:
+        raise PvlError(PVL_ERR_INVALID_ARG, "bad tile map sizes")
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=seq_id.device)
+    offs = (ctypes.c_size_t * len(TM_FIELDS))()
+    _check(lib.tile_map_layout(B, L, block_m, block_n, ctypes.addressof(offs)))
+    with torch.cuda.device(seq_id.device):
+        _check(lib.tile_map_build(seq_id.data_ptr(), B, L, block_m, block_n, ws.data_ptr(), ws.numel(),
+                                  _stream(stream)))
+    return TileMap(ws, B, L, block_m, block_n, tuple(offs))
+
+
+# ---------------------------------------------------------------- attention
+def _qkv_shape(q: torch.Tensor):
+    if q.dim() != 4:
+        raise ValueError("q must be [B, L, H, D]")
+    return tuple(q.shape)
+
+
+def masked_attn_fwd(q, k, v, seq_id, tile_map: TileMap, scale: float | None = None, o=None, lse=None,
+                    stream=None):
+    """(O bf16 [B, L, H, D], LSE fp32 [B, H, L]) of seq_id-masked softmax attention."""
+    B, L, H, D = _qkv_shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(t, name, torch.bfloat16, (B, L, H, D))
+    _need_cuda(seq_id, "seq_id", torch.int32, (B, L))
+    if (tile_map.B, tile_map.L) != (B, L):
+        raise ValueError("tile map was built for another [B, L]")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    _need_cuda(o, "o", torch.bfloat16, (B, L, H, D))
+    _need_cuda(lse, "lse", torch.float32, (B, H, L))
+    with torch.cuda.device(q.device):
+        _check(_lib.load().masked_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_id.data_ptr(),
+                                           tile_map.ws.data_ptr(), B, L, H, D, scale, o.data_ptr(),
+                                           lse.data_ptr(), _stream(stream)))
+    return o, lse
+
+
+def masked_attn_bwd_ws_bytes(B: int, L: int, H: int, D: int) -> int:
+    return int(_lib.load().masked_attn_bwd_ws_bytes(B, L, H, D))
+
+
+def masked_attn_bwd(q, k, v, o, do, lse, seq_id, tile_map: TileMap, scale: float | None = None, dq=None,
+                    dk=None, dv=None, ws=None, stream=None):
+    """(dQ, dK, dV) bf16 [B, L, H, D] of the masked attention, from the saved LSE."""
+    B, L, H, D = _qkv_shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _need_cuda(t, name, torch.bfloat16, (B, L, H, D))
+    _need_cuda(lse, "lse", torch.float32, (B, H, L))
+    _need_cuda(seq_id, "seq_id", torch.int32, (B, L))
+    if (tile_map.B, tile_map.L) != (B, L):
+        raise ValueError("tile map was built for another [B, L]")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _need_cuda(t, name, torch.bfloat16, (B, L, H, D))
+    lib = _lib.load()
+    nbytes = int(lib.masked_attn_bwd_ws_bytes(B, L, H, D))
+    if ws is None:
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        _check(lib.masked_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                   lse.data_ptr(), seq_id.data_ptr(), tile_map.ws.data_ptr(), B, L, H, D, scale,
+                                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws.numel(),
+                                   _stream(stream)))
+    return dq, dk, dv
+
+
+# ------------------------------------------------------------------- errors
+def device_error(stream=None, raise_on_error: bool = True):
+    """Synchronises the stream and returns (status, [code, where, block, thread])."""
+    info = (ctypes.c_int32 * 4)()
+    st = _lib.load().pvl_device_error_detail(_stream(stream), ctypes.addressof(info))
+    msg = _lib.load().pvl_last_error_message().decode()
+    if raise_on_error and st != PVL_OK:
+        raise PvlError(st, msg)
+    return st, list(info)
+
+
+def version() -> int:
+    return int(_lib.load().pvl_version())

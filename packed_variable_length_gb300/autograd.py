@@ -1,0 +1,35 @@
+"""torch.autograd wrapper: packed masked attention as a differentiable op.
+
+The tile map is an explicit argument of both passes, so the backward always
+sees the mask of its own forward (the class-attribute block-mask hazard of
+"lingbot_va_packing" §2.2 cannot occur).
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import api
+
+
+class _PackedAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, seq_id, tile_map, scale):
+        o, lse = api.masked_attn_fwd(q, k, v, seq_id, tile_map, scale)
+        ctx.save_for_backward(q, k, v, o, lse, seq_id)
+        ctx.tile_map = tile_map
+        ctx.scale = scale
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, seq_id = ctx.saved_tensors
+        dq, dk, dv = api.masked_attn_bwd(q, k, v, o, do.contiguous(), lse, seq_id, ctx.tile_map, ctx.scale)
+        return dq, dk, dv, None, None, None
+
+
+def packed_attention(q, k, v, seq_id, tile_map=None, scale=None):
+    """O = masked softmax attention of bf16 [B, L, H, D] q/k/v under int32 [B, L] seq_id."""
+    if tile_map is None:
+        tile_map = api.tile_map_build(seq_id)
+    return _PackedAttention.apply(q, k, v, seq_id, tile_map, scale)

@@ -1,0 +1,128 @@
+// Internal definitions shared by the host entry points and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "pvl.h"
+
+#ifdef __CUDACC__
+#define PVL_HD __host__ __device__
+#else
+#define PVL_HD
+#endif
+
+namespace pvl {
+
+// ------------------------------------------------------------ device errors
+constexpr uint32_t kDevErrTimeout = 1;  // a bounded wait ran out
+constexpr uint32_t kDevErrTileMap = 2;  // tile map header does not match the call
+
+struct DeviceError {
+  unsigned int code;
+  unsigned int where;
+  unsigned int block;
+  unsigned int thread;
+};
+
+// Default bound on any single device-side wait.
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+// --------------------------------------------------------- tile map layout
+constexpr int32_t kTileMapMagic = 0x544C5650;  // "PVLT"
+constexpr int32_t kTileMapVersion = 1;
+constexpr uint8_t kEmpty = 0, kPartial = 1, kFull = 2;
+
+struct TileMapLayout {
+  size_t off[PVL_TM_NFIELDS];
+  size_t total;
+  int nTq, nTk;
+};
+
+PVL_HD inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+PVL_HD inline TileMapLayout tile_map_layout_of(int B, int L, int bm, int bn) {
+  TileMapLayout t{};
+  t.nTq = (L + bm - 1) / bm;
+  t.nTk = (L + bn - 1) / bn;
+  const size_t nq = static_cast<size_t>(B) * t.nTq;
+  const size_t nk = static_cast<size_t>(B) * t.nTk;
+  const size_t nqk = nq * t.nTk;
+  size_t sizes[PVL_TM_NFIELDS];
+  sizes[PVL_TM_HEADER] = 16 * 4;
+  sizes[PVL_TM_Q_NV] = sizes[PVL_TM_Q_LO] = sizes[PVL_TM_Q_HI] = nq * 4;
+  sizes[PVL_TM_K_NV] = sizes[PVL_TM_K_LO] = sizes[PVL_TM_K_HI] = nk * 4;
+  sizes[PVL_TM_CLS] = nqk;
+  sizes[PVL_TM_ROW_COUNT] = sizes[PVL_TM_ROW_FULL] = nq * 4;
+  sizes[PVL_TM_ROW_LIST] = nqk * 4;
+  sizes[PVL_TM_COL_COUNT] = sizes[PVL_TM_COL_FULL] = nk * 4;
+  sizes[PVL_TM_COL_LIST] = nqk * 4;
+  sizes[PVL_TM_Q_ORDER] = nq * 4;
+  sizes[PVL_TM_K_ORDER] = nk * 4;
+  size_t pos = 0;
+  for (int i = 0; i < PVL_TM_NFIELDS; ++i) {
+    t.off[i] = pos;
+    pos = align256(pos + sizes[i]);
+  }
+  t.total = pos;
+  return t;
+}
+
+// Read-only view of a tile map the attention kernels consume.
+struct TileMapView {
+  const int32_t* header;
+  const int32_t* row_count;
+  const int32_t* row_full;
+  const int32_t* row_list;
+  const int32_t* col_count;
+  const int32_t* col_full;
+  const int32_t* col_list;
+  const int32_t* q_order;
+  const int32_t* k_order;
+  int nTq, nTk;
+};
+
+inline TileMapView tile_map_view(const void* ws, int B, int L, int bm, int bn) {
+  const TileMapLayout t = tile_map_layout_of(B, L, bm, bn);
+  const char* p = static_cast<const char*>(ws);
+  TileMapView v;
+  v.header = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_HEADER]);
+  v.row_count = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_ROW_COUNT]);
+  v.row_full = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_ROW_FULL]);
+  v.row_list = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_ROW_LIST]);
+  v.col_count = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_COL_COUNT]);
+  v.col_full = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_COL_FULL]);
+  v.col_list = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_COL_LIST]);
+  v.q_order = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_Q_ORDER]);
+  v.k_order = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_K_ORDER]);
+  v.nTq = t.nTq;
+  v.nTk = t.nTk;
+  return v;
+}
+
+// ------------------------------------------------------- host-side helpers
+// Implemented in pvl_runtime.cu.
+pvl_status fail(pvl_status s, const char* fmt, ...);
+pvl_status check_cuda(int err, const char* what);  // err is a cudaError_t
+DeviceError* device_error_record();                // current device, null on failure
+int sm_count();                                    // current device, 0 on failure
+
+// Shared argument checks of the attention calls: null pointers and sizes
+// (INVALID_ARG), D, alignment and limits (UNSUPPORTED).
+pvl_status validate_attn(const char* who, const void* const* ptrs, int nptrs, int B, int L, int H, int D, float scale);
+
+// Bytes of the backward workspace: fp32 dQ accumulator [B, L, H, D] then
+// fp32 Delta [B, H, L], each 256-byte aligned.
+inline size_t bwd_ws_dq_bytes(int B, int L, int H, int D) {
+  return align256(static_cast<size_t>(B) * L * H * D * 4);
+}
+inline size_t bwd_ws_total_bytes(int B, int L, int H, int D) {
+  return bwd_ws_dq_bytes(B, L, H, D) + align256(static_cast<size_t>(B) * H * L * 4);
+}
+
+// bf16 [B, L, H, D] tensor map with a (64 x 1 x 128 x 1) box and 128-byte
+// swizzle: one box is 128 rows of 64 features (16 KB).
+pvl_status make_bhld_tensor_map(void* map_out /* CUtensorMap* */, const void* base, int B, int L, int H,
+                                int D);
+
+}  // namespace pvl

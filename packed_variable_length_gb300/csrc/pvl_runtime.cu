@@ -1,0 +1,155 @@
+// Host runtime pieces shared by all entry points: status messages, the
+// per-device error record, SM counts and TMA tensor-map creation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "pvl_internal.h"
+
+namespace pvl {
+
+__device__ DeviceError g_device_error;
+
+namespace {
+thread_local char t_message[512] = "ok";
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceError* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+}  // namespace
+
+pvl_status fail(pvl_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_message, sizeof(t_message), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+pvl_status check_cuda(int err, const char* what) {
+  if (err == cudaSuccess) return PVL_OK;
+  return fail(PVL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(static_cast<cudaError_t>(err)));
+}
+
+DeviceError* device_error_record() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<DeviceError*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+pvl_status validate_attn(const char* who, const void* const* ptrs, int nptrs, int B, int L, int H, int D,
+                         float scale) {
+  for (int i = 0; i < nptrs; ++i)
+    if (!ptrs[i]) return fail(PVL_ERR_INVALID_ARG, "%s: pointer argument %d is null", who, i);
+  if (B < 1 || L < 1 || H < 1) return fail(PVL_ERR_INVALID_ARG, "%s: B, L and H must be >= 1", who);
+  if (!(scale > 0.0f) || !(scale < 1e30f)) return fail(PVL_ERR_INVALID_ARG, "%s: scale must be positive and finite", who);
+  if (D != 64 && D != 128) return fail(PVL_ERR_UNSUPPORTED, "%s: D = %d (supported: 64, 128)", who, D);
+  if (L > PVL_MAX_L) return fail(PVL_ERR_UNSUPPORTED, "%s: L = %d exceeds %d", who, L, PVL_MAX_L);
+  if (static_cast<long long>(B) * L * H * D >= (1ll << 40))
+    return fail(PVL_ERR_UNSUPPORTED, "%s: tensor of %lld elements is too large", who,
+                static_cast<long long>(B) * L * H * D);
+  if (static_cast<long long>(B) * ((L + 127) / 128) * H >= (1ll << 31))
+    return fail(PVL_ERR_UNSUPPORTED, "%s: too many work items", who);
+  for (int i = 0; i < nptrs; ++i)
+    if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0)
+      return fail(PVL_ERR_UNSUPPORTED, "%s: pointer argument %d is not 16-byte aligned", who, i);
+  return PVL_OK;
+}
+
+pvl_status make_bhld_tensor_map(void* map_out, const void* base, int B, int L, int H, int D) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q{};
+      const cudaError_t e =
+          cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(PVL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(L) * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PVL_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+  return PVL_OK;
+}
+
+}  // namespace pvl
+
+using namespace pvl;
+
+extern "C" pvl_status pvl_device_error_detail(pvl_stream_t stream, int32_t* info) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  pvl_status st = check_cuda(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  if (st != PVL_OK) return st;
+  DeviceError* rec = device_error_record();
+  if (!rec) return fail(PVL_ERR_CUDA, "device error record is not available");
+  DeviceError h{};
+  st = check_cuda(cudaMemcpy(&h, rec, sizeof(h), cudaMemcpyDeviceToHost), "reading the device error record");
+  if (st != PVL_OK) return st;
+  if (h.code != 0) {
+    const DeviceError zero{};
+    st = check_cuda(cudaMemcpy(rec, &zero, sizeof(zero), cudaMemcpyHostToDevice), "clearing the device error record");
+    if (st != PVL_OK) return st;
+  }
+  if (info) {
+    info[0] = static_cast<int32_t>(h.code);
+    info[1] = static_cast<int32_t>(h.where);
+    info[2] = static_cast<int32_t>(h.block);
+    info[3] = static_cast<int32_t>(h.thread);
+  }
+  if (h.code == kDevErrTimeout)
+    return fail(PVL_ERR_TIMEOUT, "device wait timed out (site %u, block %u, thread %u)", h.where, h.block, h.thread);
+  if (h.code == kDevErrTileMap)
+    return fail(PVL_ERR_INVALID_ARG, "tile map was built for another shape or block size");
+  if (h.code != 0) return fail(PVL_ERR_CUDA, "unknown device error code %u", h.code);
+  return PVL_OK;
+}
+
+extern "C" pvl_status pvl_device_error(pvl_stream_t stream) { return pvl_device_error_detail(stream, nullptr); }
+
+extern "C" const char* pvl_last_error_message(void) { return t_message; }
+
+extern "C" int pvl_version(void) { return 0x000100; }

@@ -1,0 +1,270 @@
+// tile_map_build: classify every (query tile, key tile) pair of the seq_id
+// mask as EMPTY / PARTIAL / FULL and compact the non-empty pairs into
+// per-tile work lists plus a longest-first order of the tiles.
+//
+// "lingbot_va_packing" §2.1-§2.2: FlexAttention derives a block mask from the
+// seq_ids and skips blocks with no admissible pair.  Here the map is built by
+// three small kernels on the caller's stream:
+//   1. tile_stats:  per tile, count / min / max of the valid ids;
+//   2. tile_lists:  one warp per query tile (and per key tile) classifies its
+//                   pairs from the stats and compacts FULL then PARTIAL
+//                   indices with ballots;
+//   3. tile_order:  bitonic sort in shared memory of (count desc, index asc).
+#include <cuda_runtime.h>
+
+#include "pvl_internal.h"
+
+namespace pvl {
+namespace {
+
+struct TileMapPtrs {
+  int32_t* header;
+  int32_t *q_nv, *q_lo, *q_hi, *k_nv, *k_lo, *k_hi;
+  uint8_t* cls;
+  int32_t *row_count, *row_full, *row_list, *col_count, *col_full, *col_list, *q_order, *k_order;
+};
+
+TileMapPtrs tile_map_ptrs(void* ws, const TileMapLayout& t) {
+  char* p = static_cast<char*>(ws);
+  auto i32 = [&](int f) { return reinterpret_cast<int32_t*>(p + t.off[f]); };
+  TileMapPtrs r;
+  r.header = i32(PVL_TM_HEADER);
+  r.q_nv = i32(PVL_TM_Q_NV);
+  r.q_lo = i32(PVL_TM_Q_LO);
+  r.q_hi = i32(PVL_TM_Q_HI);
+  r.k_nv = i32(PVL_TM_K_NV);
+  r.k_lo = i32(PVL_TM_K_LO);
+  r.k_hi = i32(PVL_TM_K_HI);
+  r.cls = reinterpret_cast<uint8_t*>(p + t.off[PVL_TM_CLS]);
+  r.row_count = i32(PVL_TM_ROW_COUNT);
+  r.row_full = i32(PVL_TM_ROW_FULL);
+  r.row_list = i32(PVL_TM_ROW_LIST);
+  r.col_count = i32(PVL_TM_COL_COUNT);
+  r.col_full = i32(PVL_TM_COL_FULL);
+  r.col_list = i32(PVL_TM_COL_LIST);
+  r.q_order = i32(PVL_TM_Q_ORDER);
+  r.k_order = i32(PVL_TM_K_ORDER);
+  return r;
+}
+
+constexpr int kStatThreads = 128;
+
+// grid (nTq + nTk, B): blocks [0, nTq) summarise query tiles of block_m
+// positions, the rest key tiles of block_n positions.
+__global__ void __launch_bounds__(kStatThreads) tile_stats_kernel(const int32_t* __restrict__ seq_id, int B, int L,
+                                                                  int bm, int bn, int nTq, int nTk, TileMapPtrs m) {
+  const int b = blockIdx.y;
+  const bool is_q = blockIdx.x < nTq;
+  const int t = is_q ? blockIdx.x : blockIdx.x - nTq;
+  const int bs = is_q ? bm : bn;
+  int cnt = 0, lo = INT32_MAX, hi = INT32_MIN;
+  for (int i = threadIdx.x; i < bs; i += kStatThreads) {
+    const long long p = static_cast<long long>(t) * bs + i;
+    if (p < L) {
+      const int32_t s = seq_id[static_cast<size_t>(b) * L + p];
+      if (s >= 0) {
+        ++cnt;
+        lo = min(lo, s);
+        hi = max(hi, s);
+      }
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  __shared__ int s_cnt[kStatThreads / 32], s_lo[kStatThreads / 32], s_hi[kStatThreads / 32];
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    s_cnt[w] = cnt;
+    s_lo[w] = lo;
+    s_hi[w] = hi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < kStatThreads / 32; ++i) {
+      cnt += s_cnt[i];
+      lo = min(lo, s_lo[i]);
+      hi = max(hi, s_hi[i]);
+    }
+    if (cnt == 0) lo = hi = 0;
+    const int idx = b * (is_q ? nTq : nTk) + t;
+    (is_q ? m.q_nv : m.k_nv)[idx] = cnt;
+    (is_q ? m.q_lo : m.k_lo)[idx] = lo;
+    (is_q ? m.q_hi : m.k_hi)[idx] = hi;
+    if (blockIdx.x == 0 && b == 0) {
+      m.header[0] = kTileMapMagic;
+      m.header[1] = kTileMapVersion;
+      m.header[2] = B;
+      m.header[3] = L;
+      m.header[4] = bm;
+      m.header[5] = bn;
+      m.header[6] = nTq;
+      m.header[7] = nTk;
+      for (int i = 8; i < 16; ++i) m.header[i] = 0;
+    }
+  }
+}
+
+__device__ __forceinline__ uint8_t classify(int nvq, int loq, int hiq, int bm, int nvk, int lok, int hik, int bn) {
+  if (nvq == 0 || nvk == 0 || hiq < lok || hik < loq) return kEmpty;
+  if (loq == hiq && lok == hik && loq == lok && nvq == bm && nvk == bn) return kFull;
+  return kPartial;
+}
+
+constexpr int kListWarps = 8;
+
+// One warp per list.  Warps [0, B*nTq) own query tile rows (and write CLS),
+// warps [B*nTq, B*nTq + B*nTk) own key tile columns.
+__global__ void __launch_bounds__(kListWarps * 32) tile_lists_kernel(int B, int bm, int bn, int nTq, int nTk,
+                                                                     TileMapPtrs m) {
+  const long long w = static_cast<long long>(blockIdx.x) * kListWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long long nrows = static_cast<long long>(B) * nTq;
+  const long long ncols = static_cast<long long>(B) * nTk;
+  if (w >= nrows + ncols) return;
+  const bool is_row = w < nrows;
+  const int b = static_cast<int>(is_row ? w / nTq : (w - nrows) / nTk);
+  const int t = static_cast<int>(is_row ? w % nTq : (w - nrows) % nTk);
+  const int n_other = is_row ? nTk : nTq;
+  // this tile's summary
+  const int nv0 = is_row ? m.q_nv[b * nTq + t] : m.k_nv[b * nTk + t];
+  const int lo0 = is_row ? m.q_lo[b * nTq + t] : m.k_lo[b * nTk + t];
+  const int hi0 = is_row ? m.q_hi[b * nTq + t] : m.k_hi[b * nTk + t];
+  int32_t* list = is_row ? m.row_list + (static_cast<size_t>(b) * nTq + t) * nTk
+                         : m.col_list + (static_cast<size_t>(b) * nTk + t) * nTq;
+  int written = 0, nfull = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const uint8_t want = pass == 0 ? kFull : kPartial;
+    for (int base = 0; base < n_other; base += 32) {
+      const int o = base + lane;
+      uint8_t c = kEmpty;
+      if (o < n_other) {
+        if (is_row) {
+          c = classify(nv0, lo0, hi0, bm, m.k_nv[b * nTk + o], m.k_lo[b * nTk + o], m.k_hi[b * nTk + o], bn);
+          if (pass == 0) m.cls[(static_cast<size_t>(b) * nTq + t) * nTk + o] = c;
+        } else {
+          c = classify(m.q_nv[b * nTq + o], m.q_lo[b * nTq + o], m.q_hi[b * nTq + o], bm, nv0, lo0, hi0, bn);
+        }
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, o < n_other && c == want);
+      if (c == want && o < n_other) list[written + __popc(hit & ((1u << lane) - 1u))] = o;
+      written += __popc(hit);
+    }
+    if (pass == 0) nfull = written;
+  }
+  for (int o = written + lane; o < n_other; o += 32) list[o] = -1;
+  if (lane == 0) {
+    if (is_row) {
+      m.row_count[b * nTq + t] = written;
+      m.row_full[b * nTq + t] = nfull;
+    } else {
+      m.col_count[b * nTk + t] = written;
+      m.col_full[b * nTk + t] = nfull;
+    }
+  }
+}
+
+constexpr int kOrderThreads = 1024;
+constexpr int kIdxBits = 14;  // PVL_MAX_ORDER_TILES == 1 << 14
+
+// Block 0 sorts the query tiles, block 1 the key tiles.  Key =
+// (PVL_MAX_ORDER_TILES - count) << 14 | index, ascending, so larger counts come
+// first and ties keep ascending index; padding keys are 0xFFFFFFFF.
+__global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(int nq, int nk, int npow2_q, int npow2_k,
+                                                                   TileMapPtrs m) {
+  extern __shared__ uint32_t keys[];
+  const bool is_q = blockIdx.x == 0;
+  const int n = is_q ? nq : nk;
+  const int np2 = is_q ? npow2_q : npow2_k;
+  const int32_t* cnt = is_q ? m.row_count : m.col_count;
+  int32_t* out = is_q ? m.q_order : m.k_order;
+  for (int i = threadIdx.x; i < np2; i += kOrderThreads)
+    keys[i] = i < n ? (static_cast<uint32_t>(PVL_MAX_ORDER_TILES - cnt[i]) << kIdxBits) | static_cast<uint32_t>(i)
+                    : 0xFFFFFFFFu;
+  __syncthreads();
+  for (int k = 2; k <= np2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < np2; i += kOrderThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint32_t a = keys[i], c = keys[ixj];
+          const bool ascending = (i & k) == 0;
+          if ((a > c) == ascending) {
+            keys[i] = c;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < n; i += kOrderThreads)
+    out[i] = static_cast<int32_t>(keys[i] & ((1u << kIdxBits) - 1u));
+}
+
+int next_pow2(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+}  // namespace
+}  // namespace pvl
+
+using namespace pvl;
+
+extern "C" size_t tile_map_ws_bytes(int B, int L, int block_m, int block_n) {
+  if (B < 1 || L < 1 || block_m < 1 || block_n < 1) return 0;
+  return tile_map_layout_of(B, L, block_m, block_n).total;
+}
+
+extern "C" pvl_status tile_map_layout(int B, int L, int block_m, int block_n, size_t* offsets) {
+  if (!offsets) return fail(PVL_ERR_INVALID_ARG, "tile_map_layout: null offsets");
+  if (B < 1 || L < 1 || block_m < 1 || block_n < 1)
+    return fail(PVL_ERR_INVALID_ARG, "tile_map_layout: sizes must be >= 1");
+  const TileMapLayout t = tile_map_layout_of(B, L, block_m, block_n);
+  for (int i = 0; i < PVL_TM_NFIELDS; ++i) offsets[i] = t.off[i];
+  return PVL_OK;
+}
+
+extern "C" pvl_status tile_map_build(const int32_t* seq_id, int B, int L, int block_m, int block_n, void* tile_ws,
+                                     size_t ws_bytes, pvl_stream_t stream) {
+  if (!seq_id || !tile_ws) return fail(PVL_ERR_INVALID_ARG, "tile_map_build: null pointer");
+  if (B < 1 || L < 1) return fail(PVL_ERR_INVALID_ARG, "tile_map_build: B and L must be >= 1");
+  if (block_m < 1 || block_m > 1024 || block_n < 1 || block_n > 1024)
+    return fail(PVL_ERR_UNSUPPORTED, "tile_map_build: block sizes must be in 1..1024");
+  if (L > PVL_MAX_L) return fail(PVL_ERR_UNSUPPORTED, "tile_map_build: L = %d exceeds %d", L, PVL_MAX_L);
+  if (reinterpret_cast<uintptr_t>(tile_ws) % 256 != 0)
+    return fail(PVL_ERR_INVALID_ARG, "tile_map_build: workspace must be 256-byte aligned");
+  const TileMapLayout t = tile_map_layout_of(B, L, block_m, block_n);
+  if (ws_bytes < t.total)
+    return fail(PVL_ERR_INVALID_ARG, "tile_map_build: workspace %zu bytes < %zu needed", ws_bytes, t.total);
+  const long long nq = static_cast<long long>(B) * t.nTq, nk = static_cast<long long>(B) * t.nTk;
+  if (nq > PVL_MAX_ORDER_TILES || nk > PVL_MAX_ORDER_TILES)
+    return fail(PVL_ERR_UNSUPPORTED, "tile_map_build: B * tiles = %lld exceeds %d", nq > nk ? nq : nk,
+                PVL_MAX_ORDER_TILES);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const TileMapPtrs m = tile_map_ptrs(tile_ws, t);
+
+  tile_stats_kernel<<<dim3(t.nTq + t.nTk, B), kStatThreads, 0, s>>>(seq_id, B, L, block_m, block_n, t.nTq, t.nTk, m);
+  pvl_status st = check_cuda(cudaGetLastError(), "tile_stats launch");
+  if (st != PVL_OK) return st;
+
+  const long long nwarps = nq + nk;
+  tile_lists_kernel<<<static_cast<unsigned>((nwarps + kListWarps - 1) / kListWarps), kListWarps * 32, 0, s>>>(
+      B, block_m, block_n, t.nTq, t.nTk, m);
+  st = check_cuda(cudaGetLastError(), "tile_lists launch");
+  if (st != PVL_OK) return st;
+
+  const int pq = next_pow2(static_cast<int>(nq)), pk = next_pow2(static_cast<int>(nk));
+  const int smem = (pq > pk ? pq : pk) * static_cast<int>(sizeof(uint32_t));
+  if (smem > 48 * 1024) {
+    st = check_cuda(cudaFuncSetAttribute(tile_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                    "tile_order smem attribute");
+    if (st != PVL_OK) return st;
+  }
+  tile_order_kernel<<<2, kOrderThreads, smem, s>>>(static_cast<int>(nq), static_cast<int>(nk), pq, pk, m);
+  return check_cuda(cudaGetLastError(), "tile_order launch");
+}
