@@ -1,7 +1,547 @@
-// masked_attn_bwd (kernels to come).
+// masked_attn_bwd: gradients of seq_id-masked softmax attention, sm_103a.
+//
+// What it computes (the backward of the masked attention the pages run as a
+// FlexAttention template, "lingbot_va_attn_profiling" kernel table), with
+// P_ij = M_ij exp(scale <q_i, k_j> - LSE_i) recomputed from the saved LSE:
+//   Delta_i = <dO_i, O_i>,  dS = P * (dO V^T - Delta),
+//   dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K.
+// Keys with seq_id -1 get dK = dV = 0 and queries with seq_id -1 get dQ = 0.
+//
+// Three launches on the caller's stream:
+//   bwd_pre      Delta (fp32 [B, H, L]) and a zeroed fp32 dQ accumulator;
+//   bwd_main     one persistent CTA per SM over work items (b, key tile, head)
+//                in the tile map's longest-first key order.  Per item the K/V
+//                tile stays in shared memory while the non-empty query tiles
+//                stream through (FULL first, PARTIAL last):
+//                  warp 4     TMA producer (Q_i, dO_i tiles; LSE, Delta and
+//                             query seq_ids of the tile into shared memory);
+//                  warp 5     TMEM owner and MMA issuer:
+//                             S^T = K Q_i^T, dP^T = V dO_i^T,
+//                             dV += P^T dO_i, dK += dS^T Q_i, dQ_i = dS K;
+//                  warps 0-3  thread t owns key row t: P^T and dS^T from the
+//                             TMEM rows of S^T and dP^T (mask on PARTIAL
+//                             tiles only), written bf16 to swizzled shared
+//                             memory; then adds its row of dQ_i (TMEM lane t
+//                             = query row t) into the accumulator with vector
+//                             reductions; at the end writes dK (times scale)
+//                             and dV.
+//   bwd_convert  dQ = bf16(scale * accumulator).
+// The score matrix never reaches global memory.  Every wait is bounded.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "pvl_internal.h"
+#include "pvl_device.cuh"
+
+namespace pvl {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;     // S^T            [0, 128)
+constexpr uint32_t kColDP = 128;  // dP^T, then dQ  [128, 256)
+constexpr uint32_t kColDV = 256;  // dV             [256, 256 + D)
+// dK at [256 + D, 256 + 2 D)
+
+enum BwdSite : uint32_t {
+  kSiteKvEmpty = 21, kSiteQdoEmpty, kSiteKvFull, kSiteQdoFull, kSiteDqFree, kSitePsFull, kSiteAccFree,
+  kSiteSFull, kSiteDpFull, kSiteQdoFullC, kSiteMmaDone
+};
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kQ = kV + kTile;
+  static constexpr int kDO = kQ + kTile;
+  static constexpr int kPT = kDO + kTile;       // P^T  bf16 [128 keys][128 queries]
+  static constexpr int kDST = kPT + 128 * 256;  // dS^T bf16 [128 keys][128 queries]
+  static constexpr int kEnd = kDST + 128 * 256;
+  static constexpr int kBytes = (kEnd + 1024) > 120 * 1024 ? (kEnd + 1024) : 120 * 1024;
+};
+
+struct BwdParams {
+  const int32_t* seq_id;
+  const int32_t* header;
+  const int32_t* col_count;
+  const int32_t* col_full;
+  const int32_t* col_list;
+  const int32_t* k_order;
+  const float* lse;
+  const float* delta;
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  DeviceError* err;
+  int B, L, H, nT;
+  long long total_items;
+  float scale_log2;
+  float scale;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_base, int kk) {
+  return sdesc_sw128(tile_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_base, int kk) {
+  return sdesc_sw128(tile_base + kk * 2048, 16384, 1024);
+}
+
+// ------------------------------------------------------------- preprocess
+// One group of D/8 lanes per (b, l, h) row: Delta = <dO, O> in fp32, and the
+// row's dQ accumulator set to zero.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ dO, float* __restrict__ delta,
+                                                      float* __restrict__ dq_acc, int L, int H, long long rows) {
+  constexpr int G = D / 8;
+  const int lane = threadIdx.x & 31;
+  const long long total = rows * G;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;  // a multiple of 32
+  // warp-aligned loop: every lane of a warp runs the same iterations, so the
+  // shuffles below always see the whole warp
+  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
+       base += stride) {
+    const long long t = base + lane;
+    const bool act = t < total;
+    const long long row = act ? t / G : 0;
+    const int part = static_cast<int>(t % G);
+    float s = 0.0f;
+    if (act) {
+      const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[part];
+      const uint4 c = reinterpret_cast<const uint4*>(dO + row * D)[part];
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = __bfloat1622float2(a2[i]);
+        const float2 y = __bfloat1622float2(c2[i]);
+        s = fmaf(x.x, y.x, s);
+        s = fmaf(x.y, y.y, s);
+      }
+    }
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (act) {
+      float4* acc = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
+      acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (part == 0) {
+        const long long bl = row / H;
+        const int h = static_cast<int>(row % H);
+        const long long b = bl / L;
+        const long long l = bl % L;
+        delta[(b * H + h) * L + l] = s;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ convert
+__global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restrict__ dq_acc,
+                                                          __nv_bfloat16* __restrict__ dq, float scale, long long n8) {
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = gid; i < n8; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+    uint4 out;
+    out.x = pack_bf16x2(a.x * scale, a.y * scale);
+    out.y = pack_bf16x2(a.z * scale, a.w * scale);
+    out.z = pack_bf16x2(b.x * scale, b.y * scale);
+    out.w = pack_bf16x2(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[i] = out;
+  }
+}
+
+// --------------------------------------------------------------------- main
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                    const BwdParams p) {
+  using S = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_qdo_full, bar_qdo_empty;
+  __shared__ uint64_t bar_s_full, bar_dp_full, bar_ps_full, bar_mma_done, bar_dq_free, bar_acc_free, bar_final;
+  __shared__ float lse2_s[128], delta_s[128];
+  __shared__ int32_t qseq_s[128];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nT = p.nT;
+  constexpr uint32_t kColDK = kColDV + D;
+
+  {
+    const int32_t* hd = p.header;
+    const bool ok = hd[0] == kTileMapMagic && hd[1] == kTileMapVersion && hd[2] == p.B && hd[3] == p.L &&
+                    hd[4] == 128 && hd[5] == 128;
+    if (!ok) {
+      if (threadIdx.x == 0 && atomicCAS(&p.err->code, 0u, kDevErrTileMap) == 0u) p.err->block = blockIdx.x;
+      return;
+    }
+  }
+
+  if (threadIdx.x == 0) {
+    abort_s = 0;
+    mbar_init(&bar_kv_full, 1);
+    mbar_init(&bar_kv_empty, 1);
+    mbar_init(&bar_qdo_full, 1);
+    mbar_init(&bar_qdo_empty, 1);
+    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_dp_full, 1);
+    mbar_init(&bar_ps_full, 128);
+    mbar_init(&bar_mma_done, 1);
+    mbar_init(&bar_dq_free, 128);
+    mbar_init(&bar_acc_free, 128);
+    mbar_init(&bar_final, 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_base_s, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+    tma_prefetch_desc(&tmap_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem = tmem_base_s;
+  const KernelCtl ctl{p.err, &abort_s, p.timeout_ns};
+  const uint32_t sK = smem_u32(smem + S::kK);
+  const uint32_t sV = smem_u32(smem + S::kV);
+  const uint32_t sQ = smem_u32(smem + S::kQ);
+  const uint32_t sDO = smem_u32(smem + S::kDO);
+  const uint32_t sPT = smem_u32(smem + S::kPT);
+  const uint32_t sDST = smem_u32(smem + S::kDST);
+  constexpr uint32_t kTileBytes = S::kTile;
+  constexpr float kLog2e = 1.4426950408889634f;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    uint32_t kv_it = 0, qdo_it = 0;
+    bool alive = true;
+    for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+      const int tile = p.k_order[w / p.H];
+      const int h = static_cast<int>(w % p.H);
+      const int b = tile / nT, kt = tile % nT;
+      const int n = p.col_count[tile];
+      if (n == 0) continue;
+      const int32_t* list = p.col_list + static_cast<size_t>(tile) * nT;
+      bool ok = lane == 0 ? mbar_wait(&bar_kv_empty, (kv_it & 1) ^ 1, ctl, kSiteKvEmpty) : true;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar_kv_full, 2 * kTileBytes);
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s) {
+          tma_load_4d(smem + S::kK + s * 16384, &tmap_k, &bar_kv_full, s * 64, h, kt * 128, b);
+          tma_load_4d(smem + S::kV + s * 16384, &tmap_v, &bar_kv_full, s * 64, h, kt * 128, b);
+        }
+      }
+      ++kv_it;
+      const float* lse_row = p.lse + (static_cast<size_t>(b) * p.H + h) * p.L;
+      const float* delta_row = p.delta + (static_cast<size_t>(b) * p.H + h) * p.L;
+      for (int i = 0; i < n; ++i, ++qdo_it) {
+        const int qt = list[i];
+        ok = lane == 0 ? mbar_wait(&bar_qdo_empty, (qdo_it & 1) ^ 1, ctl, kSiteQdoEmpty) : true;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int c = lane * 4 + r;
+          const int qpos = qt * 128 + c;
+          const bool in = qpos < p.L;
+          lse2_s[c] = in ? lse_row[qpos] * kLog2e : -INFINITY;
+          delta_s[c] = in ? delta_row[qpos] : 0.0f;
+          qseq_s[c] = in ? p.seq_id[static_cast<size_t>(b) * p.L + qpos] : -1;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_qdo_full, 2 * kTileBytes);
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s) {
+            tma_load_4d(smem + S::kQ + s * 16384, &tmap_q, &bar_qdo_full, s * 64, h, qt * 128, b);
+            tma_load_4d(smem + S::kDO + s * 16384, &tmap_do, &bar_qdo_full, s * 64, h, qt * 128, b);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (abort_s && lane == 0) {
+      if (kv_it > 0) mbar_drain(&bar_kv_full, (kv_it - 1) & 1, 100000000ull);
+      if (qdo_it > 0) mbar_drain(&bar_qdo_full, (qdo_it - 1) & 1, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc_st = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+    constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);    // dV, dK
+    constexpr uint32_t idesc_dq = idesc_bf16(128, D, true, true);      // dQ
+    uint32_t kv_it = 0, qdo_it = 0, item_it = 0;
+    bool alive = true;
+    auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+      bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
+      return __shfl_sync(0xffffffffu, ok, 0);
+    };
+    for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+      const int tile = p.k_order[w / p.H];
+      const int n = p.col_count[tile];
+      if (n == 0) continue;
+      if (!wait1(&bar_kv_full, kv_it & 1, kSiteKvFull)) { alive = false; break; }
+      ++kv_it;
+      for (int i = 0; i < n; ++i, ++qdo_it) {
+        if (!wait1(&bar_qdo_full, qdo_it & 1, kSiteQdoFull)) { alive = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColS, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), idesc_st, kk > 0 ? 1u : 0u);
+          umma_commit(&bar_s_full);
+        }
+        __syncwarp();
+        if (!wait1(&bar_dq_free, (qdo_it & 1) ^ 1, kSiteDqFree)) { alive = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColDP, kmajor_desc(sV, kk), kmajor_desc(sDO, kk), idesc_st, kk > 0 ? 1u : 0u);
+          umma_commit(&bar_dp_full);
+        }
+        __syncwarp();
+        if (!wait1(&bar_ps_full, qdo_it & 1, kSitePsFull)) { alive = false; break; }
+        if (i == 0 && !wait1(&bar_acc_free, (item_it & 1) ^ 1, kSiteAccFree)) { alive = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(tmem + kColDV, kmajor_desc(sPT, kk), mnmajor_desc(sDO, kk), idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(tmem + kColDK, kmajor_desc(sDST, kk), mnmajor_desc(sQ, kk), idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(tmem + kColDP, mnmajor_desc(sDST, kk), mnmajor_desc(sK, kk), idesc_dq, kk > 0 ? 1u : 0u);
+          umma_commit(&bar_mma_done);
+          umma_commit(&bar_qdo_empty);
+        }
+        __syncwarp();
+      }
+      if (!alive) break;
+      if (lane == 0) umma_commit(&bar_kv_empty);
+      __syncwarp();
+      ++item_it;
+    }
+    if (lane == 0) {
+      umma_commit(&bar_final);
+      mbar_drain(&bar_final, 0, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- compute
+    const int t = threadIdx.x;  // key row inside the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t qdo_it = 0;
+    bool alive = true;
+    auto waitw = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
+    };
+    for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+      const int tile = p.k_order[w / p.H];
+      const int h = static_cast<int>(w % p.H);
+      const int b = tile / nT, kt = tile % nT;
+      const int n = p.col_count[tile];
+      const int kpos = kt * 128 + t;
+      const bool k_in = kpos < p.L;
+      const size_t krow = ((static_cast<size_t>(b) * p.L + kpos) * p.H + h) * D;
+      if (n == 0) {  // no valid key in this tile: zero gradients
+        if (k_in) {
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            reinterpret_cast<uint4*>(p.dk + krow)[c] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(p.dv + krow)[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        continue;
+      }
+      const int nfull = p.col_full[tile];
+      const int32_t* list = p.col_list + static_cast<size_t>(tile) * nT;
+      const int my_seq = k_in ? p.seq_id[static_cast<size_t>(b) * p.L + kpos] : -1;
+      for (int i = 0; i < n; ++i, ++qdo_it) {
+        const int qt = list[i];
+        const bool partial = i >= nfull;
+        if (!waitw(&bar_s_full, qdo_it & 1, kSiteSFull)) { alive = false; break; }
+        if (!waitw(&bar_dp_full, qdo_it & 1, kSiteDpFull)) { alive = false; break; }
+        if (!waitw(&bar_qdo_full, qdo_it & 1, kSiteQdoFullC)) { alive = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rs[32], rd[32];
+          tmem_ld32(tmem + lane_base + kColS + c * 32, rs);
+          tmem_ld32(tmem + lane_base + kColDP + c * 32, rd);
+          tmem_wait_ld();
+          uint32_t pp[16], dd[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int q = c * 32 + e + u;
+              float pr = ex2(fmaf(__uint_as_float(rs[e + u]), p.scale_log2, -lse2_s[q]));
+              if (partial && (my_seq < 0 || qseq_s[q] != my_seq)) pr = 0.0f;
+              pv[u] = pr;
+              dv[u] = pr * (__uint_as_float(rd[e + u]) - delta_s[q]);
+            }
+            pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
+            dd[e / 2] = pack_bf16x2(dv[0], dv[1]);
+          }
+          const uint32_t half = static_cast<uint32_t>(c >> 1) * 16384;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t off = half + sw128_offset(t, (c & 1) * 4 + v);
+            st_shared_v4(sPT + off, pp[4 * v], pp[4 * v + 1], pp[4 * v + 2], pp[4 * v + 3]);
+            st_shared_v4(sDST + off, dd[4 * v], dd[4 * v + 1], dd[4 * v + 2], dd[4 * v + 3]);
+          }
+        }
+        const int qpos = qt * 128 + t;  // query row of dQ this thread adds
+        const bool q_live = qpos < p.L && qseq_s[t] >= 0;
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar_ps_full);
+        if (!waitw(&bar_mma_done, qdo_it & 1, kSiteMmaDone)) { alive = false; break; }
+        tc_fence_after();
+        float* dqrow = p.dq_acc + ((static_cast<size_t>(b) * p.L + qpos) * p.H + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + kColDP + c * 32, r);
+          tmem_wait_ld();
+          if (q_live) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              red_add_v4(dqrow + c * 32 + v * 4, __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                         __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bar_dq_free);
+      }
+      if (!alive) break;
+      // epilogue: the last mma_done covered every dV / dK MMA of this item
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rv[32], rk[32];
+        tmem_ld32(tmem + lane_base + kColDV + c * 32, rv);
+        tmem_ld32(tmem + lane_base + kColDK + c * 32, rk);
+        tmem_wait_ld();
+        if (k_in) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 ov, ok;
+            ov.x = pack_bf16x2(__uint_as_float(rv[8 * v + 0]), __uint_as_float(rv[8 * v + 1]));
+            ov.y = pack_bf16x2(__uint_as_float(rv[8 * v + 2]), __uint_as_float(rv[8 * v + 3]));
+            ov.z = pack_bf16x2(__uint_as_float(rv[8 * v + 4]), __uint_as_float(rv[8 * v + 5]));
+            ov.w = pack_bf16x2(__uint_as_float(rv[8 * v + 6]), __uint_as_float(rv[8 * v + 7]));
+            ok.x = pack_bf16x2(__uint_as_float(rk[8 * v + 0]) * p.scale, __uint_as_float(rk[8 * v + 1]) * p.scale);
+            ok.y = pack_bf16x2(__uint_as_float(rk[8 * v + 2]) * p.scale, __uint_as_float(rk[8 * v + 3]) * p.scale);
+            ok.z = pack_bf16x2(__uint_as_float(rk[8 * v + 4]) * p.scale, __uint_as_float(rk[8 * v + 5]) * p.scale);
+            ok.w = pack_bf16x2(__uint_as_float(rk[8 * v + 6]) * p.scale, __uint_as_float(rk[8 * v + 7]) * p.scale);
+            reinterpret_cast<uint4*>(p.dv + krow)[c * 4 + v] = ov;
+            reinterpret_cast<uint4*>(p.dk + krow)[c * 4 + v] = ok;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_acc_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+int grid_for(long long work, int threads) {
+  const int sms = sm_count();
+  long long g = (work + threads - 1) / threads;
+  const long long cap = static_cast<long long>(sms > 0 ? sms : 132) * 8;
+  if (g > cap) g = cap;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+template <int D>
+pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, const pvl_bf16* o,
+                      const pvl_bf16* dO, const float* lse, const int32_t* seq_id, const void* tile_ws, int B,
+                      int L, int H, float scale, pvl_bf16* dq, pvl_bf16* dk, pvl_bf16* dv, void* ws,
+                      cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, tdo;
+  pvl_status st = make_bhld_tensor_map(&tq, q, B, L, H, D);
+  if (st == PVL_OK) st = make_bhld_tensor_map(&tk, k, B, L, H, D);
+  if (st == PVL_OK) st = make_bhld_tensor_map(&tv, v, B, L, H, D);
+  if (st == PVL_OK) st = make_bhld_tensor_map(&tdo, dO, B, L, H, D);
+  if (st != PVL_OK) return st;
+  DeviceError* err = device_error_record();
+  const int sms = sm_count();
+  if (!err || sms <= 0) return fail(PVL_ERR_CUDA, "masked_attn_bwd: no usable CUDA device");
+
+  float* dq_acc = static_cast<float*>(ws);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(ws) + bwd_ws_dq_bytes(B, L, H, D));
+  const long long rows = static_cast<long long>(B) * L * H;
+
+  bwd_pre_kernel<D><<<grid_for(rows * (D / 8), 256), 256, 0, stream>>>(
+      reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), delta, dq_acc, L, H, rows);
+  st = check_cuda(cudaGetLastError(), "masked_attn_bwd preprocess launch");
+  if (st != PVL_OK) return st;
+
+  const TileMapView tm = tile_map_view(tile_ws, B, L, 128, 128);
+  BwdParams prm;
+  prm.seq_id = seq_id;
+  prm.header = tm.header;
+  prm.col_count = tm.col_count;
+  prm.col_full = tm.col_full;
+  prm.col_list = tm.col_list;
+  prm.k_order = tm.k_order;
+  prm.lse = lse;
+  prm.delta = delta;
+  prm.dq_acc = dq_acc;
+  prm.dk = reinterpret_cast<__nv_bfloat16*>(dk);
+  prm.dv = reinterpret_cast<__nv_bfloat16*>(dv);
+  prm.err = err;
+  prm.B = B;
+  prm.L = L;
+  prm.H = H;
+  prm.nT = tm.nTk;
+  prm.total_items = static_cast<long long>(B) * tm.nTk * H;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.scale = scale;
+  prm.timeout_ns = kDefaultTimeoutNs;
+  const int smem = BwdSmem<D>::kBytes;
+  st = check_cuda(cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                  "masked_attn_bwd smem attribute");
+  if (st != PVL_OK) return st;
+  const long long grid = prm.total_items < sms ? prm.total_items : sms;
+  bwd_main_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tq, tk, tv, tdo, prm);
+  st = check_cuda(cudaGetLastError(), "masked_attn_bwd main launch");
+  if (st != PVL_OK) return st;
+
+  const long long n8 = rows * D / 8;
+  bwd_convert_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(dq_acc, reinterpret_cast<__nv_bfloat16*>(dq), scale, n8);
+  return check_cuda(cudaGetLastError(), "masked_attn_bwd convert launch");
+}
+
+}  // namespace
+}  // namespace pvl
 
 using namespace pvl;
 
@@ -20,6 +560,9 @@ extern "C" pvl_status masked_attn_bwd(const pvl_bf16* q, const pvl_bf16* k, cons
                 masked_attn_bwd_ws_bytes(B, L, H, D));
   pvl_status st = validate_attn("masked_attn_bwd", ptrs, 12, B, L, H, D, scale);
   if (st != PVL_OK) return st;
-  (void)stream;
-  return fail(PVL_ERR_UNSUPPORTED, "masked_attn_bwd: not built yet");
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0)
+    return fail(PVL_ERR_INVALID_ARG, "masked_attn_bwd: workspace must be 256-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D == 64) return launch_bwd<64>(q, k, v, o, dO, lse, seq_id, tile_ws, B, L, H, scale, dq, dk, dv, ws, s);
+  return launch_bwd<128>(q, k, v, o, dO, lse, seq_id, tile_ws, B, L, H, scale, dq, dk, dv, ws, s);
 }

@@ -90,6 +90,16 @@ pvl_status validate_attn(const char* who, const void* const* ptrs, int nptrs, in
 }
 
 pvl_status make_bhld_tensor_map(void* map_out, const void* base, int B, int L, int H, int D) {
+  // cuTensorMapEncodeTiled is a driver call and needs a current context on
+  // this thread.  A thread that has made no runtime call yet (for example a
+  // torch autograd worker) has none; setting the current device binds the
+  // device's primary context.
+  {
+    int dev = 0;
+    pvl_status st = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+    if (st == PVL_OK) st = check_cuda(cudaSetDevice(dev), "cudaSetDevice");
+    if (st != PVL_OK) return st;
+  }
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_encode) {
