@@ -1,0 +1,401 @@
+"""Benchmark of the packed variable-length masked-attention hot path on GB300.
+
+One step = the whole path over one packed batch, every call through the
+C ABI (libpvl.so) on one stream:
+    pack_build_seq_ids -> tile_map_build -> masked_attn_fwd -> masked_attn_bwd
+Workload: the 64k concatenated pack (one row of 7 episodes with latent F
+drawn from U{103..362} rounded up to multiples of 8, 38 tokens per frame,
+tail padded with seq_id -1 to 65,536 tokens), H = 12, D = 128, bf16.
+Metric: effective TFLOP/s = 14 * D * H * (unmasked pairs) / step time, where
+a pair (i, j) is unmasked iff seq_id[i] == seq_id[j] >= 0 (forward 4 D and
+backward 10 D flops per pair and head).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the step on
+its own GPU (the path has no exchange step); rank 0 prints one JSON line.
+`--impl reference` times the fp64 CPU oracle on this host's cores instead
+(rank 0 only), on bounded samples of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective masked-attn fwd+bwd TFLOP/s and tokens/s at 1 GB300; % of bf16 peak"
+FLOPS_PER_PAIR_FWD = 4
+FLOPS_PER_PAIR_BWD = 10
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def unmasked_pairs(lay) -> int:
+    """Pairs per head: every segment's real tokens form one id (distinct ids per segment)."""
+    T = lay.tokens_per_frame
+    return int(sum(int(v) * T * int(v) * T for row in lay.seg_valid for v in row))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- GPU arm
+def dist_setup(n_gpus: int):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def traffic_record(kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh)
+    src = os.path.join(ROOT, "packed_variable_length_gb300", "csrc", kernel_file)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    entry = rec.get(kernel_file)
+    if not entry or entry.get("source_sha") != sha:
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+WORKLOADS = {"concat64k": 4, "padded": 3, "same_length": 2}
+
+
+def describe(lay, valid_tokens: int) -> str:
+    if lay.name == "concat64k":
+        return (f"concat64k: one packed row of {lay.K} episodes (latent F = {lay.seg_frames[0].tolist()}, "
+                f"{lay.tokens_per_frame} tokens/frame, {valid_tokens} valid tokens) padded with seq_id -1 to "
+                f"L = {lay.L}; H = {lay.H}, D = {lay.D}")
+    return (f"{lay.name}: B = {lay.B} episodes of valid F = {lay.seg_valid[:, 0].tolist()} padded to "
+            f"F = {int(lay.seg_frames[0, 0])} ({lay.tokens_per_frame} tokens/frame, L = {lay.L}); "
+            f"H = {lay.H}, D = {lay.D}")
+
+
+def cpu_baseline(lay, tensors, budget_heads=1):
+    """The fp64 oracle as it stands on this host's cores: fwd + bwd of one head
+    over every episode of the workload."""
+    import oracle
+    sid = oracle.build_seq_ids(lay.seg_frames, lay.seg_valid, lay.tokens_per_frame, lay.L)
+    heads = list(range(budget_heads))
+    t0 = time.perf_counter()
+    oracle.attention_fwd(tensors["q"], tensors["k"], tensors["v"], sid, heads=heads)
+    oracle.attention_bwd(tensors["q"], tensors["k"], tensors["v"], tensors["do"], sid, heads=heads)
+    dt = time.perf_counter() - t0
+    flops = (FLOPS_PER_PAIR_FWD + FLOPS_PER_PAIR_BWD) * lay.D * len(heads) * unmasked_pairs(lay)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, fwd+bwd of {len(heads)} of {lay.H} heads over all {lay.K} episodes "
+                      f"({lay.L} tokens), {dt:.1f} s; BLAS threads = host cores"}
+
+
+def run_gpu(args):
+    import torch
+    import packed_variable_length_gb300 as pvl
+    import workloads as wl
+
+    rank, world, local = dist_setup(args.gpus)
+    lay = wl.config_layout(WORKLOADS[args.workload])
+    host = wl.make_tensors(lay)  # bf16 CPU tensors, seeded
+    dev = {k: v.cuda() for k, v in host.items()}
+    B, L, H, D = lay.B, lay.L, lay.H, lay.D
+    T = lay.tokens_per_frame
+    pairs = unmasked_pairs(lay)
+    valid_tokens = int(lay.seg_valid.sum()) * T
+    flops_fwd = FLOPS_PER_PAIR_FWD * D * H * pairs
+    flops_bwd = FLOPS_PER_PAIR_BWD * D * H * pairs
+    flops = flops_fwd + flops_bwd
+
+    sid = torch.empty((B, L), dtype=torch.int32, device="cuda")
+    tm_ws = torch.empty(pvl.tile_map_ws_bytes(B, L), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(dev["q"])
+    lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    dq, dk, dv = (torch.empty_like(dev["q"]) for _ in range(3))
+    bws = torch.empty(pvl.masked_attn_bwd_ws_bytes(B, L, H, D), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(timers=None):
+        pvl.pack_build_seq_ids(lay.seg_frames, lay.seg_valid, T, L, out=sid)
+        tm = pvl.tile_map_build(sid, ws=tm_ws)
+        if timers is not None:
+            timers[0].record(stream)
+        pvl.masked_attn_fwd(dev["q"], dev["k"], dev["v"], sid, tm, o=o, lse=lse)
+        if timers is not None:
+            timers[1].record(stream)
+        pvl.masked_attn_bwd(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, sid, tm, dq=dq, dk=dk, dv=dv, ws=bws)
+        if timers is not None:
+            timers[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    pvl.device_error()
+
+    timers = [[ev(), ev(), ev()] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start, t_end = ev(), ev()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(timers[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    pvl.device_error()
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world)
+    ms_step = ms_total / args.steps
+    fwd_ms = sum(t[0].elapsed_time(t[1]) for t in timers) / args.steps
+    bwd_ms = sum(t[1].elapsed_time(t[2]) for t in timers) / args.steps
+
+    # end to end: pinned host buffers in, results back, copies inside the timed region
+    pin = {k: v.pin_memory() for k, v in host.items()}
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+
+    def e2e_step():
+        for k in ("q", "k", "v", "do"):
+            dev[k].copy_(pin[k], non_blocking=True)
+        step()
+        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            out_host[n].copy_(t, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    pvl.device_error()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("q", "k", "v", "do"))
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    bwd_achieved = flops_bwd / (bwd_ms * 1e-3) / 1e12
+    traffic = traffic_record("attn_bwd.cu")
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": describe(lay, valid_tokens),
+            "B": B, "L": L, "H": H, "D": D, "tokens_per_frame": T,
+            "unmasked_pairs_per_head": pairs,
+            "step": "pack_build_seq_ids + tile_map_build + masked_attn_fwd + masked_attn_bwd",
+            "l2": f"inputs larger than L2 (Q, K, V, dO are {dev['q'].numel() * 2 / 1e6:.0f} MB each); no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "tokens_per_s": round(world * valid_tokens / (ms_step * 1e-3), 1),
+        "padded_tokens_per_s": round(world * B * L / (ms_step * 1e-3), 1),
+        "pct_of_peak": round(100.0 * (value / world) / peak, 2),
+        "peak_tflops": peak,
+        "peak_kind": f"bf16 dense, {peaks['source']} sustained",
+        "fwd_ms": round(fwd_ms, 4),
+        "bwd_ms": round(bwd_ms, 4),
+        "fwd_tflops": round(flops_fwd / (fwd_ms * 1e-3) / 1e12, 2),
+        "bwd_tflops": round(bwd_achieved, 2),
+        "clocks": clk,
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 8 * args.steps,
+        "roofline": {
+            "kernel": "masked_attn_bwd (bwd_pre + bwd_main + bwd_convert launches, timed together)",
+            "bound": "tensor", "achieved": round(bwd_achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(bwd_achieved / peak, 4), "traffic": traffic,
+            "peak_note": f"of {peaks['source']} (bf16 cuBLAS, sustained)",
+            "algorithmic": "10 * D * H * unmasked pairs per launch",
+        },
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(lay, host)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------- reference arm
+def run_reference(args):
+    """The fp64 oracle on the host cores, one bounded sample per step: fwd + bwd
+    of one (episode, head) of the same workload, rotating over both."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    import workloads as wl
+    lay = wl.config_layout(4)
+    host = wl.make_tensors(lay)
+    T = lay.tokens_per_frame
+    starts = np.concatenate([[0], np.cumsum(lay.seg_frames[0]) * T])
+    samples = [(e, h) for h in range(lay.H) for e in range(lay.K)]
+    done_flops = 0.0
+    done_time = 0.0
+    for it in range(args.warmup + args.steps):
+        e, h = samples[it % len(samples)]
+        a, b = int(starts[e]), int(starts[e] + lay.seg_valid[0, e] * T)
+        sl = {k: v[:, a:b] for k, v in host.items()}
+        sid = np.zeros((1, b - a), np.int32)
+        t0 = time.perf_counter()
+        oracle.attention_fwd(sl["q"], sl["k"], sl["v"], sid, heads=[h])
+        oracle.attention_bwd(sl["q"], sl["k"], sl["v"], sl["do"], sid, heads=[h])
+        dt = time.perf_counter() - t0
+        if it >= args.warmup:
+            done_flops += (FLOPS_PER_PAIR_FWD + FLOPS_PER_PAIR_BWD) * lay.D * (b - a) ** 2
+            done_time += dt
+    value = done_flops / done_time / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"fp64 numpy oracle: each step is fwd+bwd of one (episode, head) of the concat64k workload "
+              f"(rotating over {lay.K} episodes x {lay.H} heads); {args.steps} timed steps, {done_time:.1f} s")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * done_time / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "concat64k (same as the GPU arm), sampled per (episode, head)",
+                   "B": lay.B, "L": lay.L, "H": lay.H, "D": lay.D},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="concat64k", choices=sorted(WORKLOADS),
+                    help="concat64k is the headline workload; the others are smaller cases for profiling")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("bench.py: raising --warmup to 3 (the minimum for a valid timing)", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
