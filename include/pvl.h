@@ -179,6 +179,41 @@ PVL_API pvl_status masked_attn_bwd(const pvl_bf16* q, const pvl_bf16* k, const p
                            void* ws, size_t ws_bytes, pvl_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * masked_attn_bwd_no_alloc — masked_attn_bwd for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this entry point
+ * exists for the caller, not for the method.
+ *
+ * Some callers are handed only their input and output buffers and may not
+ * call cudaMalloc: a plug-in inside a framework that has reserved the whole
+ * device memory pool for its own allocator, or a latency-bound loop where an
+ * allocation (which can synchronise the device) is not allowed.  This call
+ * computes exactly what masked_attn_bwd computes, with the same arguments
+ * minus the workspace: its scratch (fp32 dQ accumulator and Delta) lives in
+ * one static device array of PVL_NO_ALLOC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads the library holds until the process exits.  It
+ * calls no allocating routine.
+ *
+ * Limit: masked_attn_bwd_ws_bytes(B, L, H, D) (about B*L*H*(D+1)*4 bytes)
+ *   must not exceed PVL_NO_ALLOC_SCRATCH_BYTES; larger shapes return
+ *   PVL_ERR_UNSUPPORTED without launching anything.
+ * Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * Sharing: all calls on a device use the same array.  Each call clears what
+ *   must start at zero, so earlier contents do not matter, but calls whose
+ *   work overlaps on the GPU (other streams, other threads) race on the
+ *   scratch and give wrong gradients: serialise them.
+ * Errors: as masked_attn_bwd.
+ * ---------------------------------------------------------------------- */
+#define PVL_NO_ALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+
+PVL_API pvl_status masked_attn_bwd_no_alloc(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v,
+                                            const pvl_bf16* o, const pvl_bf16* dO, const float* lse,
+                                            const int32_t* seq_id, const void* tile_ws, int B, int L, int H, int D,
+                                            float scale, pvl_bf16* dq, pvl_bf16* dk, pvl_bf16* dv,
+                                            pvl_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Device error record.  Synchronises `stream`, reads and clears the current
  * device's error record.  Returns PVL_OK, PVL_ERR_TIMEOUT (a bounded wait ran
  * out; the kernel released its resources and returned), PVL_ERR_INVALID_ARG

@@ -15,6 +15,7 @@ from .api import (  # noqa: F401
     TileMap,
     device_error,
     masked_attn_bwd,
+    masked_attn_bwd_no_alloc,
     masked_attn_bwd_ws_bytes,
     masked_attn_fwd,
     pack_build_seq_ids,

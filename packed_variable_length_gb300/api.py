@@ -200,6 +200,34 @@ def masked_attn_bwd(q, k, v, o, do, lse, seq_id, tile_map: TileMap, scale: float
     return dq, dk, dv
 
 
+def masked_attn_bwd_no_alloc(q, k, v, o, do, lse, seq_id, tile_map: TileMap, scale: float | None = None,
+                             dq=None, dk=None, dv=None, stream=None):
+    """masked_attn_bwd without a workspace argument, for callers that must not
+    allocate device memory: the scratch is the library's own static device
+    array (limit PVL_NO_ALLOC_SCRATCH_BYTES).  Pass dq/dk/dv to avoid the
+    output allocations too.  Calls that overlap on the GPU share that scratch
+    and must be serialised."""
+    B, L, H, D = _qkv_shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _need_cuda(t, name, torch.bfloat16, (B, L, H, D))
+    _need_cuda(lse, "lse", torch.float32, (B, H, L))
+    _need_cuda(seq_id, "seq_id", torch.int32, (B, L))
+    if (tile_map.B, tile_map.L) != (B, L):
+        raise ValueError("tile map was built for another [B, L]")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _need_cuda(t, name, torch.bfloat16, (B, L, H, D))
+    with torch.cuda.device(q.device):
+        _check(_lib.load().masked_attn_bwd_no_alloc(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+            seq_id.data_ptr(), tile_map.ws.data_ptr(), B, L, H, D, scale, dq.data_ptr(), dk.data_ptr(),
+            dv.data_ptr(), _stream(stream)))
+    return dq, dk, dv
+
+
 # ------------------------------------------------------------------- errors
 def device_error(stream=None, raise_on_error: bool = True):
     """Synchronises the stream and returns (status, [code, where, block, thread])."""

@@ -30,6 +30,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "pvl_device.cuh"
 
 namespace pvl {
@@ -565,4 +567,63 @@ extern "C" pvl_status masked_attn_bwd(const pvl_bf16* q, const pvl_bf16* k, cons
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (D == 64) return launch_bwd<64>(q, k, v, o, dO, lse, seq_id, tile_ws, B, L, H, scale, dq, dk, dv, ws, s);
   return launch_bwd<128>(q, k, v, o, dO, lse, seq_id, tile_ws, B, L, H, scale, dq, dk, dv, ws, s);
+}
+
+// ------------------------------------------------------------------------
+// masked_attn_bwd_no_alloc: the same backward for callers that cannot
+// allocate device memory.  Its scratch (fp32 dQ accumulator and Delta) lives
+// in this file-scope array instead of a caller-provided workspace.
+namespace pvl {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(PVL_NO_ALLOC_SCRATCH_BYTES);
+
+// Held by every GPU that loads the library until the process exits.
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_no_alloc_mu;
+void* g_no_alloc_ptr[64] = {};
+
+// Device address of the scratch array on the current device.  Host code only
+// sees a host-side stand-in under the array's name, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+pvl_status no_alloc_scratch(void** out) {
+  int dev = -1;
+  pvl_status st = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != PVL_OK) return st;
+  if (dev < 0 || dev >= 64) return fail(PVL_ERR_UNSUPPORTED, "masked_attn_bwd_no_alloc: device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_no_alloc_mu);
+  if (!g_no_alloc_ptr[dev]) {
+    void* p = nullptr;
+    st = check_cuda(cudaGetSymbolAddress(&p, g_no_alloc_scratch), "cudaGetSymbolAddress(scratch)");
+    if (st != PVL_OK) return st;
+    g_no_alloc_ptr[dev] = p;
+  }
+  *out = g_no_alloc_ptr[dev];
+  return PVL_OK;
+}
+
+}  // namespace
+}  // namespace pvl
+
+extern "C" pvl_status masked_attn_bwd_no_alloc(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v,
+                                               const pvl_bf16* o, const pvl_bf16* dO, const float* lse,
+                                               const int32_t* seq_id, const void* tile_ws, int B, int L, int H,
+                                               int D, float scale, pvl_bf16* dq, pvl_bf16* dk, pvl_bf16* dv,
+                                               pvl_stream_t stream) {
+  const void* ptrs[] = {q, k, v, o, dO, lse, seq_id, tile_ws, dq, dk, dv};
+  pvl_status st = validate_attn("masked_attn_bwd_no_alloc", ptrs, 11, B, L, H, D, scale);
+  if (st != PVL_OK) return st;
+  const size_t need = masked_attn_bwd_ws_bytes(B, L, H, D);
+  if (need > kNoAllocScratchBytes)
+    return fail(PVL_ERR_UNSUPPORTED,
+                "masked_attn_bwd_no_alloc: this shape needs %zu bytes of scratch; the library's static scratch "
+                "holds %zu bytes (B*L*H*(D+1)*4 must fit); use masked_attn_bwd with a workspace instead",
+                need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  st = no_alloc_scratch(&scratch);
+  if (st != PVL_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D == 64) return launch_bwd<64>(q, k, v, o, dO, lse, seq_id, tile_ws, B, L, H, scale, dq, dk, dv, scratch, s);
+  return launch_bwd<128>(q, k, v, o, dO, lse, seq_id, tile_ws, B, L, H, scale, dq, dk, dv, scratch, s);
 }
