@@ -109,6 +109,11 @@ PVL_API pvl_status pack_build_seq_ids(const int32_t* seg_frames, const int32_t* 
  *                              by ascending index (longest work first)
  *   K_ORDER     int32[B*nTk]  the same over key tiles by COL_COUNT
  * nTq = ceil(L / block_m), nTk = ceil(L / block_n).
+ *
+ * The workspace holds PVL_TM_LEVELS such maps built from the same seq_ids:
+ * level 0 at (block_m, block_n) and level 1 at (2*block_m, block_n), whose
+ * query tiles are pairs of level-0 query tiles (the forward processes a pair
+ * of query tiles against one stream of key tiles).
  * ---------------------------------------------------------------------- */
 enum {
   PVL_TM_HEADER = 0,
@@ -120,12 +125,15 @@ enum {
   PVL_TM_Q_ORDER, PVL_TM_K_ORDER,
   PVL_TM_NFIELDS
 };
+#define PVL_TM_LEVELS 2
 
-/* Bytes of workspace for tile_map_build; 0 if the arguments are invalid. */
+/* Bytes of workspace for tile_map_build (both levels); 0 if the arguments
+ * are invalid. */
 PVL_API size_t tile_map_ws_bytes(int B, int L, int block_m, int block_n);
 
-/* Byte offsets of the PVL_TM_NFIELDS arrays inside the workspace (host call,
- * no device work).  offsets: host size_t[PVL_TM_NFIELDS]. */
+/* Byte offsets of the arrays inside the workspace (host call, no device
+ * work).  offsets: host size_t[PVL_TM_LEVELS * PVL_TM_NFIELDS]; entry
+ * level * PVL_TM_NFIELDS + field. */
 PVL_API pvl_status tile_map_layout(int B, int L, int block_m, int block_n, size_t* offsets);
 
 /* seq_id: dev int32 [B * L].  block_m, block_n in 1..1024 (the attention

@@ -20,6 +20,7 @@ from . import _lib
 PVL_OK, PVL_ERR_INVALID_ARG, PVL_ERR_UNSUPPORTED, PVL_ERR_CUDA, PVL_ERR_TIMEOUT = range(5)
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT"}
 
+TM_LEVELS = 2
 TM_FIELDS = ["header", "q_nv", "q_lo", "q_hi", "k_nv", "k_lo", "k_hi", "cls", "row_count", "row_full",
              "row_list", "col_count", "col_full", "col_list", "q_order", "k_order"]
 EMPTY, PARTIAL, FULL = 0, 1, 2
@@ -78,39 +79,52 @@ def pack_build_seq_ids(seg_frames, seg_valid, tokens_per_frame: int, L: int, out
 # ----------------------------------------------------------------- tile map
 @dataclass
 class TileMap:
-    """Device workspace written by tile_map_build plus typed views of its arrays."""
+    """Device workspace written by tile_map_build plus typed views of its arrays.
+
+    Level 0 is the map at (block_m, block_n); level 1 the map at
+    (2 * block_m, block_n) over pairs of query tiles."""
     ws: torch.Tensor
     B: int
     L: int
     block_m: int
     block_n: int
-    offsets: tuple
+    offsets: tuple  # LEVELS * len(TM_FIELDS) byte offsets
+
+    def blocks(self, level: int = 0):
+        return (self.block_m * (2 if level else 1), self.block_n)
+
+    def n_tiles(self, level: int = 0):
+        bm, bn = self.blocks(level)
+        return -(-self.L // bm), -(-self.L // bn)
 
     @property
     def nTq(self) -> int:
-        return -(-self.L // self.block_m)
+        return self.n_tiles(0)[0]
 
     @property
     def nTk(self) -> int:
-        return -(-self.L // self.block_n)
+        return self.n_tiles(0)[1]
 
-    def field(self, name: str) -> torch.Tensor:
+    def field(self, name: str, level: int = 0) -> torch.Tensor:
         i = TM_FIELDS.index(name)
-        B, nq, nk = self.B, self.nTq, self.nTk
+        B = self.B
+        nq, nk = self.n_tiles(level)
         shapes = {"header": (16,), "q_nv": (B, nq), "q_lo": (B, nq), "q_hi": (B, nq), "k_nv": (B, nk),
                   "k_lo": (B, nk), "k_hi": (B, nk), "cls": (B, nq, nk), "row_count": (B, nq),
                   "row_full": (B, nq), "row_list": (B, nq, nk), "col_count": (B, nk), "col_full": (B, nk),
                   "col_list": (B, nk, nq), "q_order": (B * nq,), "k_order": (B * nk,)}
         shape = shapes[name]
         n = int(np.prod(shape))
-        off = self.offsets[i]
+        off = self.offsets[level * len(TM_FIELDS) + i]
         if name == "cls":
             return self.ws[off:off + n].view(shape)
         return self.ws[off:off + 4 * n].view(torch.int32).view(shape)
 
-    def to_host(self) -> dict:
-        out = {name: self.field(name).cpu().numpy() for name in TM_FIELDS}
-        out.update(B=self.B, L=self.L, block_m=self.block_m, block_n=self.block_n, nTq=self.nTq, nTk=self.nTk)
+    def to_host(self, level: int = 0) -> dict:
+        out = {name: self.field(name, level).cpu().numpy() for name in TM_FIELDS}
+        bm, bn = self.blocks(level)
+        nq, nk = self.n_tiles(level)
+        out.update(B=self.B, L=self.L, block_m=bm, block_n=bn, nTq=nq, nTk=nk)
         return out
 
 
@@ -130,7 +144,7 @@ def tile_map_build(seq_id: torch.Tensor, block_m: int = 128, block_n: int = 128,
         raise PvlError(PVL_ERR_INVALID_ARG, "bad tile map sizes")
     if ws is None:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=seq_id.device)
-    offs = (ctypes.c_size_t * len(TM_FIELDS))()
+    offs = (ctypes.c_size_t * (TM_LEVELS * len(TM_FIELDS)))()
     _check(lib.tile_map_layout(B, L, block_m, block_n, ctypes.addressof(offs)))
     with torch.cuda.device(seq_id.device):
         _check(lib.tile_map_build(seq_id.data_ptr(), B, L, block_m, block_n, ws.data_ptr(), ws.numel(),

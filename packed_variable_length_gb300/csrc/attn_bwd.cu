@@ -506,7 +506,7 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   st = check_cuda(cudaGetLastError(), "masked_attn_bwd preprocess launch");
   if (st != PVL_OK) return st;
 
-  const TileMapView tm = tile_map_view(tile_ws, B, L, 128, 128);
+  const TileMapView tm = tile_map_view(tile_ws, B, L, 128, 128, 0);
   BwdParams prm;
   prm.seq_id = seq_id;
   prm.header = tm.header;

@@ -7,23 +7,29 @@
 //   LSE_i = log sum_{j: s_j = s_i} exp(scale * <q_i, k_j>);
 // rows with s_i = -1 get O_i = 0 and LSE_i = -inf.
 //
-// Design.  One persistent CTA per SM walks work items (b, query tile, head) in
-// the tile map's longest-first order, round-robin over CTAs.  Per item only
-// the key tiles the tile map lists as non-empty are touched, FULL ones first
-// (no per-element mask), then PARTIAL ones (mask from the key seq_ids).
-//   warp 4      TMA producer: Q tile once per item, K/V tiles into a 2-stage
-//               ring; for PARTIAL tiles it also stages the key seq_ids.
-//   warp 5      owns TMEM (512 columns) and issues tcgen05.mma from one
-//               thread: S = Q K^T into one of two TMEM S buffers (so S_{j+1}
-//               runs while the softmax works on S_j), then O += P V.
-//   warps 0-3   softmax: thread t owns query row t (TMEM lane t), loads its S
-//               row, applies the mask on PARTIAL tiles, keeps a running max
-//               and sum, writes P (bf16) to shared memory in the 128-byte
-//               swizzled layout the MMA reads, and rescales O in TMEM only
-//               when its running max grows by more than 2^8 (the stale max
-//               bounds every P by 256, and the final division uses the same
-//               max, so the result is unchanged).  The epilogue divides by
-//               the row sum and writes O (bf16) and LSE (fp32).
+// Design.  One persistent CTA per SM walks work items (b, query-tile pair,
+// head): two adjacent 128-row query tiles A and B that share one stream of
+// key tiles, taken from level 1 of the tile map (256-row query tiles) in its
+// longest-first order, round-robin over CTAs.  Only the key tiles the map
+// lists as non-empty are touched, FULL ones first (no per-element mask),
+// then PARTIAL ones (mask from the seq_ids).
+//   warp 8      TMA producer: the Q pair once per item, K and V tiles into
+//               separate 2-stage rings (a K stage frees as soon as both S
+//               MMAs that read it are done).
+//   warp 9      owns TMEM (512 columns: S_A, S_B, O_A, O_B) and issues
+//               tcgen05.mma from one thread in the order
+//               PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ...
+//               so the tensor core works on one query tile while the other
+//               tile's softmax runs.  PV reads P straight from TMEM.
+//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: thread t owns
+//               query row t (TMEM lane t).  Pass 1 takes the row max of S;
+//               pass 2 re-reads S, applies the mask (PARTIAL tiles only),
+//               computes P = exp2(scale*log2e*S - m), accumulates the row
+//               sum and writes P as packed bf16 over the first 64 columns of
+//               the same S buffer.  O is rescaled in TMEM only when the
+//               running max grows by more than 2^8 (the stale max bounds
+//               every P by 256 and the final division uses the same max).
+//               The epilogue divides by the row sum and writes O and LSE.
 // Every wait is bounded; on expiry the CTA records the failure, drains its
 // outstanding copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -34,27 +40,27 @@
 namespace pvl {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;  // warps 0-7 softmax (two groups), 8 TMA, 9 MMA
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;   // O accumulator columns [256, 256 + D)
+constexpr uint32_t kColS = 0;    // S_X at [128 X, 128 X + 128); P_X packed over its first 64 columns
+constexpr uint32_t kColO = 256;  // O_X at [256 + X D, 256 + (X + 1) D)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum FwdSite : uint32_t {
-  kSiteQEmpty = 1, kSiteKvEmpty, kSiteQFull, kSiteKFull, kSiteSFree, kSitePFull, kSiteVFull, kSiteOFree,
-  kSiteSFull, kSitePvDone, kSiteKseq, kSiteFinal
+  kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull, kSitePFull, kSiteOFree,
+  kSiteSFull, kSitePvDone
 };
 
 template <int D>
 struct FwdSmem {
   static constexpr int kTile = 128 * D * 2;  // one 128 x D bf16 tile (D / 64 swizzled 16 KB blocks)
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;
+  static constexpr int kQ = 0;               // Q_A then Q_B
+  static constexpr int kK = kQ + 2 * kTile;
   static constexpr int kV = kK + kStages * kTile;
-  static constexpr int kP = kV + kStages * kTile;  // 128 x 128 bf16 probabilities
-  static constexpr int kEnd = kP + 128 * 128 * 2;
+  static constexpr int kEnd = kV + kStages * kTile;
   // 1 KB alignment slack; never below 120 KB so two CTAs can not share an SM
   // (each CTA allocates all 512 TMEM columns).
   static constexpr int kBytes = (kEnd + 1024) > 120 * 1024 ? (kEnd + 1024) : 120 * 1024;
@@ -62,7 +68,7 @@ struct FwdSmem {
 
 struct FwdParams {
   const int32_t* seq_id;
-  const int32_t* header;
+  const int32_t* header;     // level-1 map (256-row query tiles)
   const int32_t* row_count;
   const int32_t* row_full;
   const int32_t* row_list;
@@ -70,7 +76,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   DeviceError* err;
-  int B, L, H, nT;
+  int B, L, H, nP, nK;       // query-tile pairs and key tiles per row
   long long total_items;
   float scale_log2;
   uint64_t timeout_ns;
@@ -88,6 +94,32 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_base, int kk) {
   return sdesc_sw128(tile_base + kk * 2048, 16384, 1024);
 }
 
+// Admissibility of keys kt*128 + 32w .. +31 for a query with id my_seq, as a
+// 32-bit mask (bit c = key kt*128 + 32w + c may be attended).
+__device__ __forceinline__ uint32_t key_mask_word(const int32_t* __restrict__ seq_row, int L, int kt, int w,
+                                                  int my_seq) {
+  if (my_seq < 0) return 0u;
+  const int k0 = kt * 128 + 32 * w;
+  uint32_t bits = 0;
+  if (k0 + 32 <= L && (reinterpret_cast<uintptr_t>(seq_row + k0) & 15u) == 0) {
+    const int4* src = reinterpret_cast<const int4*>(seq_row + k0);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const int4 s4 = __ldg(src + v);
+      bits |= (s4.x == my_seq ? 1u : 0u) << (4 * v);
+      bits |= (s4.y == my_seq ? 1u : 0u) << (4 * v + 1);
+      bits |= (s4.z == my_seq ? 1u : 0u) << (4 * v + 2);
+      bits |= (s4.w == my_seq ? 1u : 0u) << (4 * v + 3);
+    }
+  } else {
+    for (int c = 0; c < 32; ++c) {
+      const int kpos = k0 + c;
+      if (kpos < L && __ldg(seq_row + kpos) == my_seq) bits |= 1u << c;
+    }
+  }
+  return bits;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -95,22 +127,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   using S = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q_full, bar_q_empty, bar_p_full, bar_pv_done, bar_o_free, bar_final;
-  __shared__ uint64_t bar_k_full[kStages], bar_v_full[kStages], bar_kv_empty[kStages];
-  __shared__ uint64_t bar_s_full[2], bar_s_free[2];
-  __shared__ int32_t kseq_s[kStages][128];
+  __shared__ uint64_t bar_q_full, bar_q_empty, bar_o_free, bar_final;
+  __shared__ uint64_t bar_k_full[kStages], bar_k_empty[kStages], bar_v_full[kStages], bar_v_empty[kStages];
+  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nT = p.nT;
+  const int nP = p.nP, nK = p.nK;
 
   // The tile map must describe this call; otherwise do nothing.
   {
     const int32_t* hd = p.header;
     const bool ok = hd[0] == kTileMapMagic && hd[1] == kTileMapVersion && hd[2] == p.B && hd[3] == p.L &&
-                    hd[4] == 128 && hd[5] == 128;
+                    hd[4] == 256 && hd[5] == 128;
     if (!ok) {
       if (threadIdx.x == 0 && atomicCAS(&p.err->code, 0u, kDevErrTileMap) == 0u) p.err->block = blockIdx.x;
       return;
@@ -121,18 +152,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_s = 0;
     mbar_init(&bar_q_full, 1);
     mbar_init(&bar_q_empty, 1);
-    mbar_init(&bar_p_full, 128);
-    mbar_init(&bar_pv_done, 1);
-    mbar_init(&bar_o_free, 128);
+    mbar_init(&bar_o_free, 256);
     mbar_init(&bar_final, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_k_full[s], 1);
+      mbar_init(&bar_k_empty[s], 1);
       mbar_init(&bar_v_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
+      mbar_init(&bar_v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_s_free[s], 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_s_full[x], 1);
+      mbar_init(&bar_p_full[x], 128);
+      mbar_init(&bar_pv_done[x], 1);
     }
     fence_barrier_init();
   }
@@ -154,52 +185,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + S::kQ);
   const uint32_t sK0 = smem_u32(smem + S::kK);
   const uint32_t sV0 = smem_u32(smem + S::kV);
-  const uint32_t sP = smem_u32(smem + S::kP);
   constexpr uint32_t kTileBytes = S::kTile;
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     uint32_t kv_it = 0, q_it = 0;
     bool alive = true;
+    auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+      bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
+      return __shfl_sync(0xffffffffu, ok, 0);
+    };
     for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
       const int tile = p.q_order[w / p.H];
       const int h = static_cast<int>(w % p.H);
-      const int b = tile / nT, qt = tile % nT;
+      const int b = tile / nP, pp = tile % nP;
       const int n = p.row_count[tile];
       if (n == 0) continue;
-      const int nfull = p.row_full[tile];
-      const int32_t* list = p.row_list + static_cast<size_t>(tile) * nT;
-      bool ok = lane == 0 ? mbar_wait(&bar_q_empty, (q_it & 1) ^ 1, ctl, kSiteQEmpty) : true;
-      if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
+      const int32_t* list = p.row_list + static_cast<size_t>(tile) * nK;
+      if (!wait1(&bar_q_empty, (q_it & 1) ^ 1, kSiteQEmpty)) { alive = false; break; }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_q_full, kTileBytes);
+        mbar_arrive_expect_tx(&bar_q_full, 2 * kTileBytes);
 #pragma unroll
-        for (int s = 0; s < D / 64; ++s) tma_load_4d(smem + S::kQ + s * 16384, &tmap_q, &bar_q_full, s * 64, h, qt * 128, b);
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(smem + S::kQ + x * kTileBytes + s * 16384, &tmap_q, &bar_q_full, s * 64, h,
+                        pp * 256 + x * 128, b);
       }
+      __syncwarp();
       ++q_it;
       for (int j = 0; j < n; ++j, ++kv_it) {
         const int kt = list[j];
         const int st = kv_it % kStages;
-        ok = lane == 0 ? mbar_wait(&bar_kv_empty[st], ((kv_it / kStages) & 1) ^ 1, ctl, kSiteKvEmpty) : true;
-        if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
-        if (j >= nfull) {  // PARTIAL: stage the key seq_ids for the mask
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int c = lane * 4 + r;
-            const int kpos = kt * 128 + c;
-            kseq_s[st][c] = kpos < p.L ? p.seq_id[static_cast<size_t>(b) * p.L + kpos] : -1;
-          }
-        }
-        __syncwarp();
+        const uint32_t ph = ((kv_it / kStages) & 1) ^ 1;
+        if (!wait1(&bar_k_empty[st], ph, kSiteKEmpty)) { alive = false; break; }
         if (lane == 0) {
-          uint8_t* kdst = smem + S::kK + st * kTileBytes;
-          uint8_t* vdst = smem + S::kV + st * kTileBytes;
           mbar_arrive_expect_tx(&bar_k_full[st], kTileBytes);
 #pragma unroll
-          for (int s = 0; s < D / 64; ++s) tma_load_4d(kdst + s * 16384, &tmap_k, &bar_k_full[st], s * 64, h, kt * 128, b);
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(smem + S::kK + st * kTileBytes + s * 16384, &tmap_k, &bar_k_full[st], s * 64, h, kt * 128, b);
+        }
+        __syncwarp();
+        if (!wait1(&bar_v_empty[st], ph, kSiteVEmpty)) { alive = false; break; }
+        if (lane == 0) {
           mbar_arrive_expect_tx(&bar_v_full[st], kTileBytes);
 #pragma unroll
-          for (int s = 0; s < D / 64; ++s) tma_load_4d(vdst + s * 16384, &tmap_v, &bar_v_full[st], s * 64, h, kt * 128, b);
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(smem + S::kV + st * kTileBytes + s * 16384, &tmap_v, &bar_v_full[st], s * 64, h, kt * 128, b);
         }
         __syncwarp();
       }
@@ -207,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (abort_s && lane == 0) {
       // let copies still in flight land before the CTA leaves
       if (q_it > 0) mbar_drain(&bar_q_full, (q_it - 1) & 1, 100000000ull);
-      for (uint32_t it = kv_it > kStages ? kv_it - kStages : 0; it < kv_it; ++it) {
+      for (uint32_t it = kv_it > kStages ? kv_it - kStages : 0; it <= kv_it; ++it) {
         mbar_drain(&bar_k_full[it % kStages], (it / kStages) & 1, 100000000ull);
         mbar_drain(&bar_v_full[it % kStages], (it / kStages) & 1, 100000000ull);
       }
@@ -217,11 +249,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
     constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
-    uint32_t kv_it = 0, q_it = 0, s_it = 0, p_it = 0, o_it = 0;
+    uint32_t kv_it = 0, q_it = 0, p_it = 0, o_it = 0;
     bool alive = true;
     auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
       bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
       return __shfl_sync(0xffffffffu, ok, 0);
+    };
+    auto issue_s = [&](int x, uint32_t idx) {  // S_x = Q_x K^T (K stage of key tile idx)
+      const int st = idx % kStages;
+      const uint32_t qbase = sQ + x * kTileBytes;
+      const uint32_t kbase = sK0 + st * kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma_ss(tmem + kColS + x * 128, kmajor_desc(qbase, kk), kmajor_desc(kbase, kk), idesc_s, kk > 0 ? 1u : 0u);
+      umma_commit(&bar_s_full[x]);
+    };
+    auto issue_pv = [&](int x, uint32_t idx, bool accumulate) {  // O_x += P_x V (P_x in TMEM)
+      const int st = idx % kStages;
+      const uint32_t vbase = sV0 + st * kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ts(tmem + kColO + x * D, tmem + kColS + x * 128 + kk * 8, mnmajor_desc(vbase, kk), idesc_o,
+                (accumulate || kk > 0) ? 1u : 0u);
+      umma_commit(&bar_pv_done[x]);
     };
     for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
       const int tile = p.q_order[w / p.H];
@@ -229,50 +279,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n == 0) continue;
       if (!wait1(&bar_q_full, q_it & 1, kSiteQFull)) { alive = false; break; }
       ++q_it;
-      const uint32_t kv_base = kv_it;
-      // S_j = Q K_j^T into S buffer (s_it & 1)
-      auto issue_s = [&](int j) -> bool {
-        const uint32_t idx = kv_base + j;
-        const int st = idx % kStages;
-        if (!wait1(&bar_k_full[st], (idx / kStages) & 1, kSiteKFull)) return false;
-        const uint32_t sb = s_it & 1;
-        if (!wait1(&bar_s_free[sb], ((s_it >> 1) & 1) ^ 1, kSiteSFree)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t kbase = sK0 + st * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + sb * 128, kmajor_desc(sQ, kk), kmajor_desc(kbase, kk), idesc_s, kk > 0 ? 1u : 0u);
-          umma_commit(&bar_s_full[sb]);
-        }
-        __syncwarp();
-        ++s_it;
-        return true;
-      };
-      if (!issue_s(0)) { alive = false; break; }
+      const uint32_t base = kv_it;
+      if (!wait1(&bar_k_full[base % kStages], (base / kStages) & 1, kSiteKFull)) { alive = false; break; }
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(0, base);
+        issue_s(1, base);
+        umma_commit(&bar_k_empty[base % kStages]);
+      }
+      __syncwarp();
       for (int j = 0; j < n; ++j) {
-        if (j + 1 < n && !issue_s(j + 1)) { alive = false; break; }
-        const uint32_t idx = kv_base + j;
-        const int st = idx % kStages;
-        if (!wait1(&bar_p_full, p_it & 1, kSitePFull)) { alive = false; break; }
-        ++p_it;
-        if (!wait1(&bar_v_full[st], (idx / kStages) & 1, kSiteVFull)) { alive = false; break; }
+        const uint32_t idx = base + j;
+        const bool more = j + 1 < n;
+        if (!wait1(&bar_v_full[idx % kStages], (idx / kStages) & 1, kSiteVFull)) { alive = false; break; }
+        if (!wait1(&bar_p_full[0], p_it & 1, kSitePFull)) { alive = false; break; }
         if (j == 0) {
           if (!wait1(&bar_o_free, (o_it & 1) ^ 1, kSiteOFree)) { alive = false; break; }
           ++o_it;
         }
+        if (more && !wait1(&bar_k_full[(idx + 1) % kStages], ((idx + 1) / kStages) & 1, kSiteKFull)) {
+          alive = false;
+          break;
+        }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t vbase = sV0 + st * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(tmem + kTmemO, kmajor_desc(sP, kk), mnmajor_desc(vbase, kk), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&bar_pv_done);
-          umma_commit(&bar_kv_empty[st]);
+          issue_pv(0, idx, j > 0);
+          if (more) issue_s(0, idx + 1);
         }
         __syncwarp();
+        if (!wait1(&bar_p_full[1], p_it & 1, kSitePFull)) { alive = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv(1, idx, j > 0);
+          umma_commit(&bar_v_empty[idx % kStages]);
+          if (more) {
+            issue_s(1, idx + 1);
+            umma_commit(&bar_k_empty[(idx + 1) % kStages]);
+          }
+        }
+        __syncwarp();
+        ++p_it;
       }
-      kv_it = kv_base + n;
+      kv_it = base + n;
       if (!alive) break;
       if (lane == 0) umma_commit(&bar_q_empty);
       __syncwarp();
@@ -285,9 +333,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax
-    const int row = threadIdx.x;  // query row inside the tile == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t s_it = 0, pv_it = 0, kv_it = 0;
+    const int x = warp >> 2;            // query tile of the pair: 0 = A, 1 = B
+    const int row = threadIdx.x & 127;  // query row inside the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_col = tmem + lane_base + kColS + x * 128;
+    const uint32_t o_col = tmem + lane_base + kColO + x * D;
+    uint32_t s_it = 0, pv_it = 0;
     bool alive = true;
     auto waitw = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
@@ -295,13 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
       const int tile = p.q_order[w / p.H];
       const int h = static_cast<int>(w % p.H);
-      const int b = tile / nT, qt = tile % nT;
+      const int b = tile / nP, pp = tile % nP;
       const int n = p.row_count[tile];
-      const int qpos = qt * 128 + row;
+      const int qpos = pp * 256 + x * 128 + row;
       const bool in_range = qpos < p.L;
       __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.L + qpos) * p.H + h) * D;
       float* lse_out = p.lse + (static_cast<size_t>(b) * p.H + h) * p.L + qpos;
-      if (n == 0) {  // no valid query in this tile
+      if (n == 0) {  // no valid query in this pair of tiles
         if (in_range) {
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
@@ -310,93 +361,91 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int nfull = p.row_full[tile];
-      const int my_seq = in_range ? p.seq_id[static_cast<size_t>(b) * p.L + qpos] : -1;
+      const int32_t* list = p.row_list + static_cast<size_t>(tile) * nK;
+      const int32_t* seq_row = p.seq_id + static_cast<size_t>(b) * p.L;
+      const int my_seq = in_range ? seq_row[qpos] : -1;
       float m_ref = -INFINITY;  // running max of scale*log2(e)*s
-      float l = 0.0f;           // running sum of 2^(...) w.r.t. m_ref
-      for (int j = 0; j < n; ++j, ++kv_it) {
-        const uint32_t sb = s_it & 1;
-        if (!waitw(&bar_s_full[sb], (s_it >> 1) & 1, kSiteSFull)) { alive = false; break; }
+      float l = 0.0f;           // running sum of 2^(...) relative to m_ref
+      for (int j = 0; j < n; ++j) {
+        const bool partial = j >= nfull;
+        const int kt = partial ? list[j] : 0;
+        if (!waitw(&bar_s_full[x], s_it & 1, kSiteSFull)) { alive = false; break; }
+        ++s_it;
         tc_fence_after();
-        float s[128];
+        // pass 1: row max
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_base + sb * 128 + c * 32, r);
+          tmem_ld32(s_col + 32 * c, r);
+          const uint32_t mk = partial ? key_mask_word(seq_row, p.L, kt, c, my_seq) : ~0u;
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i)
+            mx4[i & 3] = fmaxf(mx4[i & 3], (mk >> i) & 1u ? __uint_as_float(r[i]) : -INFINITY);
         }
-        tc_fence_before();
-        mbar_arrive(&bar_s_free[sb]);
-        ++s_it;
-        if (j >= nfull) {  // PARTIAL tile: per-element seq_id mask
-          const int st = kv_it % kStages;
-          if (!waitw(&bar_k_full[st], (kv_it / kStages) & 1, kSiteKseq)) { alive = false; break; }
-          const int32_t* ks = kseq_s[st];
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (my_seq < 0 || ks[c] != my_seq) s[c] = -INFINITY;
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        const float mx2 = mx * p.scale_log2;
+        const float mx2 = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
         const bool grow = mx2 > m_ref + kRescaleThreshold;
         const float m_new = grow ? mx2 : m_ref;
         const float alpha = grow ? ex2(m_ref - m_new) : 1.0f;
-        l *= alpha;
-        if (j > 0) {  // PV_{j-1} done: O is stable and the P buffer is free
-          if (!waitw(&bar_pv_done, pv_it & 1, kSitePvDone)) { alive = false; break; }
+        const bool any = m_new != -INFINITY;
+        const float neg_m = any ? -m_new : 0.0f;
+        // pass 2: P = 2^(scale*log2e*S - m), packed bf16 over S columns [0, 64)
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(s_col + 32 * c, r);
+          uint32_t mk = !any ? 0u : partial ? key_mask_word(seq_row, p.L, kt, c, my_seq) : ~0u;
+          asm volatile("" : "+r"(mk));  // recomputed here rather than kept live from pass 1
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const bool k0 = (mk >> e) & 1u;
+            const bool k1 = (mk >> (e + 1)) & 1u;
+            const float p0 = k0 ? ex2(fmaf(__uint_as_float(r[e]), p.scale_log2, neg_m)) : 0.0f;
+            const float p1 = k1 ? ex2(fmaf(__uint_as_float(r[e + 1]), p.scale_log2, neg_m)) : 0.0f;
+            l4[(e >> 1) & 3] += p0 + p1;
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(s_col + 16 * c, pk);
+        }
+        l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+        // PV_x of the previous key tile has completed (S_x of this tile was
+        // issued after it); rescale O_x when the max grew.
+        if (j > 0) {
+          if (!waitw(&bar_pv_done[x], pv_it & 1, kSitePvDone)) { alive = false; break; }
           ++pv_it;
-          tc_fence_after();
           const bool rescale = grow && m_ref != -INFINITY;
           if (__any_sync(0xffffffffu, rescale)) {
             const float f = rescale ? alpha : 1.0f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               uint32_t r[32];
-              tmem_ld32(tmem + lane_base + kTmemO + c * 32, r);
+              tmem_ld32(o_col + c * 32, r);
               tmem_wait_ld();
 #pragma unroll
               for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-              tmem_st32(tmem + lane_base + kTmemO + c * 32, r);
+              tmem_st32(o_col + c * 32, r);
             }
-            tmem_wait_st();
           }
         }
         m_ref = m_new;
-        const float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;
-        const bool any = m_ref != -INFINITY;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = half * 64 + ch * 8 + e * 2;
-              const float p0 = any ? ex2(fmaf(s[c], p.scale_log2, neg_m)) : 0.0f;
-              const float p1 = any ? ex2(fmaf(s[c + 1], p.scale_log2, neg_m)) : 0.0f;
-              l += p0 + p1;
-              pk[e] = pack_bf16x2(p0, p1);
-            }
-            st_shared_v4(sP + half * 16384 + sw128_offset(row, ch), pk[0], pk[1], pk[2], pk[3]);
-          }
-        }
-        fence_async_smem();
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bar_p_full);
+        mbar_arrive(&bar_p_full[x]);
       }
       if (!alive) break;
-      // epilogue: the last PV has finished
-      if (!waitw(&bar_pv_done, pv_it & 1, kSitePvDone)) { alive = false; break; }
+      // epilogue: the last PV_x has finished
+      if (!waitw(&bar_pv_done[x], pv_it & 1, kSitePvDone)) { alive = false; break; }
       ++pv_it;
       tc_fence_after();
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_base + kTmemO + c * 32, r);
+        tmem_ld32(o_col + c * 32, r);
         tmem_wait_ld();
         if (in_range) {
 #pragma unroll
@@ -436,7 +485,7 @@ pvl_status launch_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   DeviceError* err = device_error_record();
   const int sms = sm_count();
   if (!err || sms <= 0) return fail(PVL_ERR_CUDA, "masked_attn_fwd: no usable CUDA device");
-  const TileMapView tm = tile_map_view(tile_ws, B, L, 128, 128);
+  const TileMapView tm = tile_map_view(tile_ws, B, L, 128, 128, 1);  // pairs of query tiles
   FwdParams prm;
   prm.seq_id = seq_id;
   prm.header = tm.header;
@@ -450,7 +499,8 @@ pvl_status launch_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   prm.B = B;
   prm.L = L;
   prm.H = H;
-  prm.nT = tm.nTq;
+  prm.nP = tm.nTq;
+  prm.nK = tm.nTk;
   prm.total_items = static_cast<long long>(B) * tm.nTq * H;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.timeout_ns = kDefaultTimeoutNs;

@@ -33,15 +33,16 @@ constexpr int32_t kTileMapMagic = 0x544C5650;  // "PVLT"
 constexpr int32_t kTileMapVersion = 1;
 constexpr uint8_t kEmpty = 0, kPartial = 1, kFull = 2;
 
+PVL_HD inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 struct TileMapLayout {
-  size_t off[PVL_TM_NFIELDS];
-  size_t total;
+  size_t off[PVL_TM_NFIELDS];  // absolute byte offsets inside the workspace
+  size_t total;                // end of this level
   int nTq, nTk;
 };
 
-PVL_HD inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
-PVL_HD inline TileMapLayout tile_map_layout_of(int B, int L, int bm, int bn) {
+// One level of the map (block sizes bm x bn), starting at byte `base`.
+PVL_HD inline TileMapLayout tile_map_level_layout(int B, int L, int bm, int bn, size_t base) {
   TileMapLayout t{};
   t.nTq = (L + bm - 1) / bm;
   t.nTk = (L + bn - 1) / bn;
@@ -59,7 +60,7 @@ PVL_HD inline TileMapLayout tile_map_layout_of(int B, int L, int bm, int bn) {
   sizes[PVL_TM_COL_LIST] = nqk * 4;
   sizes[PVL_TM_Q_ORDER] = nq * 4;
   sizes[PVL_TM_K_ORDER] = nk * 4;
-  size_t pos = 0;
+  size_t pos = base;
   for (int i = 0; i < PVL_TM_NFIELDS; ++i) {
     t.off[i] = pos;
     pos = align256(pos + sizes[i]);
@@ -68,9 +69,25 @@ PVL_HD inline TileMapLayout tile_map_layout_of(int B, int L, int bm, int bn) {
   return t;
 }
 
-// Read-only view of a tile map the attention kernels consume.
+// The workspace holds PVL_TM_LEVELS maps: level 0 at (bm, bn), level 1 at
+// (2 bm, bn) -- the query-tile pairs the forward kernel processes together.
+struct TileMapLayouts {
+  TileMapLayout level[PVL_TM_LEVELS];
+  size_t total;
+};
+
+PVL_HD inline TileMapLayouts tile_map_layouts(int B, int L, int bm, int bn) {
+  TileMapLayouts r{};
+  r.level[0] = tile_map_level_layout(B, L, bm, bn, 0);
+  r.level[1] = tile_map_level_layout(B, L, 2 * bm, bn, r.level[0].total);
+  r.total = r.level[1].total;
+  return r;
+}
+
+// Read-only view of one level of a tile map.
 struct TileMapView {
   const int32_t* header;
+  const uint8_t* cls;
   const int32_t* row_count;
   const int32_t* row_full;
   const int32_t* row_list;
@@ -82,11 +99,12 @@ struct TileMapView {
   int nTq, nTk;
 };
 
-inline TileMapView tile_map_view(const void* ws, int B, int L, int bm, int bn) {
-  const TileMapLayout t = tile_map_layout_of(B, L, bm, bn);
+inline TileMapView tile_map_view(const void* ws, int B, int L, int bm, int bn, int level) {
+  const TileMapLayout t = tile_map_layouts(B, L, bm, bn).level[level];
   const char* p = static_cast<const char*>(ws);
   TileMapView v;
   v.header = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_HEADER]);
+  v.cls = reinterpret_cast<const uint8_t*>(p + t.off[PVL_TM_CLS]);
   v.row_count = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_ROW_COUNT]);
   v.row_full = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_ROW_FULL]);
   v.row_list = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_ROW_LIST]);

@@ -217,15 +217,16 @@ using namespace pvl;
 
 extern "C" size_t tile_map_ws_bytes(int B, int L, int block_m, int block_n) {
   if (B < 1 || L < 1 || block_m < 1 || block_n < 1) return 0;
-  return tile_map_layout_of(B, L, block_m, block_n).total;
+  return tile_map_layouts(B, L, block_m, block_n).total;
 }
 
 extern "C" pvl_status tile_map_layout(int B, int L, int block_m, int block_n, size_t* offsets) {
   if (!offsets) return fail(PVL_ERR_INVALID_ARG, "tile_map_layout: null offsets");
   if (B < 1 || L < 1 || block_m < 1 || block_n < 1)
     return fail(PVL_ERR_INVALID_ARG, "tile_map_layout: sizes must be >= 1");
-  const TileMapLayout t = tile_map_layout_of(B, L, block_m, block_n);
-  for (int i = 0; i < PVL_TM_NFIELDS; ++i) offsets[i] = t.off[i];
+  const TileMapLayouts t = tile_map_layouts(B, L, block_m, block_n);
+  for (int lv = 0; lv < PVL_TM_LEVELS; ++lv)
+    for (int i = 0; i < PVL_TM_NFIELDS; ++i) offsets[lv * PVL_TM_NFIELDS + i] = t.level[lv].off[i];
   return PVL_OK;
 }
 
@@ -238,33 +239,40 @@ extern "C" pvl_status tile_map_build(const int32_t* seq_id, int B, int L, int bl
   if (L > PVL_MAX_L) return fail(PVL_ERR_UNSUPPORTED, "tile_map_build: L = %d exceeds %d", L, PVL_MAX_L);
   if (reinterpret_cast<uintptr_t>(tile_ws) % 256 != 0)
     return fail(PVL_ERR_INVALID_ARG, "tile_map_build: workspace must be 256-byte aligned");
-  const TileMapLayout t = tile_map_layout_of(B, L, block_m, block_n);
-  if (ws_bytes < t.total)
-    return fail(PVL_ERR_INVALID_ARG, "tile_map_build: workspace %zu bytes < %zu needed", ws_bytes, t.total);
-  const long long nq = static_cast<long long>(B) * t.nTq, nk = static_cast<long long>(B) * t.nTk;
-  if (nq > PVL_MAX_ORDER_TILES || nk > PVL_MAX_ORDER_TILES)
-    return fail(PVL_ERR_UNSUPPORTED, "tile_map_build: B * tiles = %lld exceeds %d", nq > nk ? nq : nk,
+  const TileMapLayouts all = tile_map_layouts(B, L, block_m, block_n);
+  if (ws_bytes < all.total)
+    return fail(PVL_ERR_INVALID_ARG, "tile_map_build: workspace %zu bytes < %zu needed", ws_bytes, all.total);
+  const long long nq0 = static_cast<long long>(B) * all.level[0].nTq, nk0 = static_cast<long long>(B) * all.level[0].nTk;
+  if (nq0 > PVL_MAX_ORDER_TILES || nk0 > PVL_MAX_ORDER_TILES)
+    return fail(PVL_ERR_UNSUPPORTED, "tile_map_build: B * tiles = %lld exceeds %d", nq0 > nk0 ? nq0 : nk0,
                 PVL_MAX_ORDER_TILES);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const TileMapPtrs m = tile_map_ptrs(tile_ws, t);
+  for (int lv = 0; lv < PVL_TM_LEVELS; ++lv) {
+    const TileMapLayout& t = all.level[lv];
+    const int bm = lv == 0 ? block_m : 2 * block_m;
+    const long long nq = static_cast<long long>(B) * t.nTq, nk = static_cast<long long>(B) * t.nTk;
+    const TileMapPtrs m = tile_map_ptrs(tile_ws, t);
 
-  tile_stats_kernel<<<dim3(t.nTq + t.nTk, B), kStatThreads, 0, s>>>(seq_id, B, L, block_m, block_n, t.nTq, t.nTk, m);
-  pvl_status st = check_cuda(cudaGetLastError(), "tile_stats launch");
-  if (st != PVL_OK) return st;
+    tile_stats_kernel<<<dim3(t.nTq + t.nTk, B), kStatThreads, 0, s>>>(seq_id, B, L, bm, block_n, t.nTq, t.nTk, m);
+    pvl_status st = check_cuda(cudaGetLastError(), "tile_stats launch");
+    if (st != PVL_OK) return st;
 
-  const long long nwarps = nq + nk;
-  tile_lists_kernel<<<static_cast<unsigned>((nwarps + kListWarps - 1) / kListWarps), kListWarps * 32, 0, s>>>(
-      B, block_m, block_n, t.nTq, t.nTk, m);
-  st = check_cuda(cudaGetLastError(), "tile_lists launch");
-  if (st != PVL_OK) return st;
+    const long long nwarps = nq + nk;
+    tile_lists_kernel<<<static_cast<unsigned>((nwarps + kListWarps - 1) / kListWarps), kListWarps * 32, 0, s>>>(
+        B, bm, block_n, t.nTq, t.nTk, m);
+    st = check_cuda(cudaGetLastError(), "tile_lists launch");
+    if (st != PVL_OK) return st;
 
-  const int pq = next_pow2(static_cast<int>(nq)), pk = next_pow2(static_cast<int>(nk));
-  const int smem = (pq > pk ? pq : pk) * static_cast<int>(sizeof(uint32_t));
-  if (smem > 48 * 1024) {
-    st = check_cuda(cudaFuncSetAttribute(tile_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
-                    "tile_order smem attribute");
+    const int pq = next_pow2(static_cast<int>(nq)), pk = next_pow2(static_cast<int>(nk));
+    const int smem = (pq > pk ? pq : pk) * static_cast<int>(sizeof(uint32_t));
+    if (smem > 48 * 1024) {
+      st = check_cuda(cudaFuncSetAttribute(tile_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                      "tile_order smem attribute");
+      if (st != PVL_OK) return st;
+    }
+    tile_order_kernel<<<2, kOrderThreads, smem, s>>>(static_cast<int>(nq), static_cast<int>(nk), pq, pk, m);
+    st = check_cuda(cudaGetLastError(), "tile_order launch");
     if (st != PVL_OK) return st;
   }
-  tile_order_kernel<<<2, kOrderThreads, smem, s>>>(static_cast<int>(nq), static_cast<int>(nk), pq, pk, m);
-  return check_cuda(cudaGetLastError(), "tile_order launch");
+  return PVL_OK;
 }

@@ -72,13 +72,14 @@ def test_host_validation_without_gpu(lib):
 
 def test_tile_map_layout_host(lib):
     import numpy as np
-    offs = (ctypes.c_size_t * 16)()
+    offs = (ctypes.c_size_t * 32)()
     assert lib.tile_map_layout(2, 1000, 128, 64, ctypes.addressof(offs)) == 0
     o = list(offs)
     assert o[0] == 0 and all(b > a for a, b in zip(o, o[1:])) and all(x % 256 == 0 for x in o)
     total = lib.tile_map_ws_bytes(2, 1000, 128, 64)
-    nq, nk = 2 * 8, 2 * 16
+    nq, nk = 2 * 8, 2 * 16          # level 0: 128-row query tiles, 64-key tiles
+    assert o[8] - o[7] >= nq * 16   # level-0 cls bytes
+    assert o[16 + 8] - o[16 + 7] >= 2 * 4 * 16   # level-1 cls: 256-row query tiles
     assert total >= o[-1] + 4 * nk
-    assert o[8] - o[7] >= nq * 16   # cls bytes
     assert lib.masked_attn_bwd_ws_bytes(2, 1000, 3, 128) >= 2 * 1000 * 3 * 128 * 4
     assert np.int64(lib.pvl_version()) > 0

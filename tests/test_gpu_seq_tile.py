@@ -48,7 +48,8 @@ def test_seq_ids_and_tile_map_bit_exact(pvl, lay):
     np.testing.assert_array_equal(sid.cpu().numpy(), ref_sid)
     tm = pvl.tile_map_build(sid, 128, 128)
     torch.cuda.synchronize()
-    compare_tile_maps(tm.to_host(), oracle.build_tile_map(ref_sid, lay.L, 128, 128))
+    compare_tile_maps(tm.to_host(0), oracle.build_tile_map(ref_sid, lay.L, 128, 128))
+    compare_tile_maps(tm.to_host(1), oracle.build_tile_map(ref_sid, lay.L, 256, 128))
 
 
 @pytest.mark.parametrize("seed,bm,bn", [(0, 8, 8), (1, 16, 8), (2, 8, 32), (3, 64, 128), (4, 1, 1)])
@@ -59,7 +60,8 @@ def test_tile_map_interleaved_ids(pvl, seed, bm, bn):
     sid = torch.from_numpy(ids).cuda()
     tm = pvl.tile_map_build(sid, bm, bn)
     torch.cuda.synchronize()
-    compare_tile_maps(tm.to_host(), oracle.build_tile_map(ids, L, bm, bn))
+    compare_tile_maps(tm.to_host(0), oracle.build_tile_map(ids, L, bm, bn))
+    compare_tile_maps(tm.to_host(1), oracle.build_tile_map(ids, L, 2 * bm, bn))
 
 
 def test_tile_map_large_order(pvl):
