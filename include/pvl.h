@@ -176,7 +176,8 @@ PVL_API pvl_status masked_attn_fwd(const pvl_bf16* q, const pvl_bf16* k, const p
  * forward.  dq, dk, dv: dev bf16 [B, L, H, D], fully written; rows with
  * seq_id -1 get exact zeros.
  * ws: dev scratch of masked_attn_bwd_ws_bytes(B, L, H, D) bytes, 256-byte
- *   aligned (fp32 dQ accumulator and Delta); contents on entry are ignored.
+ *   aligned (fp32 dQ accumulator; Delta, LSE*log2(e) and query seq_ids padded
+ *   to whole 128-row tiles); contents on entry are ignored.
  * Errors: as masked_attn_fwd, plus INVALID_ARG for a short workspace.
  * ---------------------------------------------------------------------- */
 PVL_API size_t masked_attn_bwd_ws_bytes(int B, int L, int H, int D);
@@ -201,7 +202,7 @@ PVL_API pvl_status masked_attn_bwd(const pvl_bf16* q, const pvl_bf16* k, const p
  * which every GPU that loads the library holds until the process exits.  It
  * calls no allocating routine.
  *
- * Limit: masked_attn_bwd_ws_bytes(B, L, H, D) (about B*L*H*(D+1)*4 bytes)
+ * Limit: masked_attn_bwd_ws_bytes(B, L, H, D) (about B*L*H*(D+2)*4 bytes)
  *   must not exceed PVL_NO_ALLOC_SCRATCH_BYTES; larger shapes return
  *   PVL_ERR_UNSUPPORTED without launching anything.
  * Set-up: the first call on a device looks up the array's device address

@@ -8,23 +8,29 @@
 // Keys with seq_id -1 get dK = dV = 0 and queries with seq_id -1 get dQ = 0.
 //
 // Three launches on the caller's stream:
-//   bwd_pre      Delta (fp32 [B, H, L]) and a zeroed fp32 dQ accumulator;
+//   bwd_pre      Delta and LSE * log2(e) per query (fp32, padded to whole
+//                128-row tiles), the padded query seq_ids, and a zeroed fp32
+//                dQ accumulator;
 //   bwd_main     one persistent CTA per SM over work items (b, key tile, head)
 //                in the tile map's longest-first key order.  Per item the K/V
 //                tile stays in shared memory while the non-empty query tiles
-//                stream through (FULL first, PARTIAL last):
-//                  warp 4     TMA producer (Q_i, dO_i tiles; LSE, Delta and
-//                             query seq_ids of the tile into shared memory);
-//                  warp 5     TMEM owner and MMA issuer:
-//                             S^T = K Q_i^T, dP^T = V dO_i^T,
-//                             dV += P^T dO_i, dK += dS^T Q_i, dQ_i = dS K;
-//                  warps 0-3  thread t owns key row t: P^T and dS^T from the
-//                             TMEM rows of S^T and dP^T (mask on PARTIAL
-//                             tiles only), written bf16 to swizzled shared
-//                             memory; then adds its row of dQ_i (TMEM lane t
-//                             = query row t) into the accumulator with vector
-//                             reductions; at the end writes dK (times scale)
-//                             and dV.
+//                stream through a 2-stage Q/dO ring (FULL first, PARTIAL last):
+//                  warp 8     TMA producer (K/V per item, Q_i and dO_i per tile);
+//                  warp 9     TMEM owner and MMA issuer:
+//                             S^T = K Q_i^T, dP^T = V dO_i^T, then
+//                             dQ_i = dS K, dV += P^T dO_i, dK += dS^T Q_i;
+//                  warps 0-7  two warpgroups over the same 128 key rows
+//                             (thread row = TMEM lane), each owning half of
+//                             the query columns and half of the feature
+//                             columns: P^T = exp2(S^T scale log2e - LSE log2e)
+//                             and dS^T = P^T (dP^T - Delta) (mask on PARTIAL
+//                             tiles only); P^T goes back into TMEM over S^T
+//                             (the dV MMA reads it from there), dS^T into
+//                             swizzled shared memory (the dQ and dK MMAs read
+//                             it); then each adds half of its row of dQ_i
+//                             (TMEM lane = query row) into the accumulator
+//                             with vector reductions; at the end each writes
+//                             half of dK (times scale) and dV.
 //   bwd_convert  dQ = bf16(scale * accumulator).
 // The score matrix never reaches global memory.  Every wait is bounded.
 #include <cuda.h>
@@ -37,18 +43,20 @@
 namespace pvl {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;  // warps 0-7 compute, 8 TMA, 9 MMA
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kComputeThreads = 256;
+constexpr int kStages = 2;        // Q/dO ring
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;     // S^T            [0, 128)
+constexpr uint32_t kColS = 0;     // S^T            [0, 128); P^T packed over [64 g, 64 g + 32)
 constexpr uint32_t kColDP = 128;  // dP^T, then dQ  [128, 256)
 constexpr uint32_t kColDV = 256;  // dV             [256, 256 + D)
 // dK at [256 + D, 256 + 2 D)
 
 enum BwdSite : uint32_t {
   kSiteKvEmpty = 21, kSiteQdoEmpty, kSiteKvFull, kSiteQdoFull, kSiteDqFree, kSitePsFull, kSiteAccFree,
-  kSiteSFull, kSiteDpFull, kSiteQdoFullC, kSiteMmaDone
+  kSiteSFull, kSiteDpFull, kSiteMmaDone, kSiteDqReady
 };
 
 template <int D>
@@ -56,28 +64,28 @@ struct BwdSmem {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
-  static constexpr int kQ = kV + kTile;
-  static constexpr int kDO = kQ + kTile;
-  static constexpr int kPT = kDO + kTile;       // P^T  bf16 [128 keys][128 queries]
-  static constexpr int kDST = kPT + 128 * 256;  // dS^T bf16 [128 keys][128 queries]
+  static constexpr int kQ = kV + kTile;            // kStages tiles
+  static constexpr int kDO = kQ + kStages * kTile;  // kStages tiles
+  static constexpr int kDST = kDO + kStages * kTile;  // dS^T bf16 [128 keys][128 queries]
   static constexpr int kEnd = kDST + 128 * 256;
   static constexpr int kBytes = (kEnd + 1024) > 120 * 1024 ? (kEnd + 1024) : 120 * 1024;
 };
 
 struct BwdParams {
-  const int32_t* seq_id;
   const int32_t* header;
   const int32_t* col_count;
   const int32_t* col_full;
   const int32_t* col_list;
   const int32_t* k_order;
-  const float* lse;
-  const float* delta;
+  const int32_t* seq_id;  // [B, L]     key seq_ids
+  const float* delta;     // [B, H, Lp]
+  const float* lse2;      // [B, H, Lp] LSE * log2(e)
+  const int32_t* qseq;    // [B, Lp]    query seq_ids, -1 past L
   float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   DeviceError* err;
-  int B, L, H, nT;
+  int B, L, Lp, H, nT;
   long long total_items;
   float scale_log2;
   float scale;
@@ -92,14 +100,19 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_base, int kk) {
 }
 
 // ------------------------------------------------------------- preprocess
-// One group of D/8 lanes per (b, l, h) row: Delta = <dO, O> in fp32, and the
-// row's dQ accumulator set to zero.
+// One group of D/8 lanes per (b, l, h) row: Delta = <dO, O> in fp32,
+// LSE * log2(e), the row's query seq_id (h = 0), and the row's dQ accumulator
+// set to zero.  Then the padding positions L <= l < Lp of the padded arrays.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
-                                                      const __nv_bfloat16* __restrict__ dO, float* __restrict__ delta,
-                                                      float* __restrict__ dq_acc, int L, int H, long long rows) {
+                                                      const __nv_bfloat16* __restrict__ dO,
+                                                      const float* __restrict__ lse, const int32_t* __restrict__ seq_id,
+                                                      float* __restrict__ delta, float* __restrict__ lse2,
+                                                      int32_t* __restrict__ qseq, float* __restrict__ dq_acc, int B,
+                                                      int L, int Lp, int H) {
   constexpr int G = D / 8;
   const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(B) * L * H;
   const long long total = rows * G;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;  // a multiple of 32
   // warp-aligned loop: every lane of a warp runs the same iterations, so the
@@ -135,9 +148,19 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
         const int h = static_cast<int>(row % H);
         const long long b = bl / L;
         const long long l = bl % L;
-        delta[(b * H + h) * L + l] = s;
+        delta[(b * H + h) * Lp + l] = s;
+        lse2[(b * H + h) * Lp + l] = lse[(b * H + h) * L + l] * 1.4426950408889634f;
+        if (h == 0) qseq[b * Lp + l] = seq_id[b * L + l];
       }
     }
+  }
+  const long long pad = static_cast<long long>(B) * H * (Lp - L);
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < pad; t += stride) {
+    const long long bh = t / (Lp - L);
+    const long long l = L + t % (Lp - L);
+    delta[bh * Lp + l] = 0.0f;
+    lse2[bh * Lp + l] = 0.0f;
+    if (bh % H == 0) qseq[(bh / H) * Lp + l] = -1;
   }
 }
 
@@ -167,10 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using S = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_qdo_full, bar_qdo_empty;
-  __shared__ uint64_t bar_s_full, bar_dp_full, bar_ps_full, bar_mma_done, bar_dq_free, bar_acc_free, bar_final;
-  __shared__ float lse2_s[128], delta_s[128];
-  __shared__ int32_t qseq_s[128];
+  __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_qdo_full[kStages], bar_qdo_empty[kStages];
+  __shared__ uint64_t bar_s_full, bar_dp_full, bar_ps_full, bar_mma_done, bar_dq_ready, bar_dq_free, bar_acc_free,
+      bar_final;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -193,14 +215,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_s = 0;
     mbar_init(&bar_kv_full, 1);
     mbar_init(&bar_kv_empty, 1);
-    mbar_init(&bar_qdo_full, 1);
-    mbar_init(&bar_qdo_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_qdo_full[s], 1);
+      mbar_init(&bar_qdo_empty[s], 1);
+    }
     mbar_init(&bar_s_full, 1);
     mbar_init(&bar_dp_full, 1);
-    mbar_init(&bar_ps_full, 128);
+    mbar_init(&bar_ps_full, kComputeThreads);
     mbar_init(&bar_mma_done, 1);
-    mbar_init(&bar_dq_free, 128);
-    mbar_init(&bar_acc_free, 128);
+    mbar_init(&bar_dq_ready, 1);
+    mbar_init(&bar_dq_free, kComputeThreads);
+    mbar_init(&bar_acc_free, kComputeThreads);
     mbar_init(&bar_final, 1);
     fence_barrier_init();
   }
@@ -222,17 +247,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const KernelCtl ctl{p.err, &abort_s, p.timeout_ns};
   const uint32_t sK = smem_u32(smem + S::kK);
   const uint32_t sV = smem_u32(smem + S::kV);
-  const uint32_t sQ = smem_u32(smem + S::kQ);
-  const uint32_t sDO = smem_u32(smem + S::kDO);
-  const uint32_t sPT = smem_u32(smem + S::kPT);
+  const uint32_t sQ0 = smem_u32(smem + S::kQ);
+  const uint32_t sDO0 = smem_u32(smem + S::kDO);
   const uint32_t sDST = smem_u32(smem + S::kDST);
   constexpr uint32_t kTileBytes = S::kTile;
-  constexpr float kLog2e = 1.4426950408889634f;
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
-    uint32_t kv_it = 0, qdo_it = 0;
+    uint32_t kv_it = 0, qi = 0;
     bool alive = true;
+    auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+      bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
+      return __shfl_sync(0xffffffffu, ok, 0);
+    };
     for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
       const int tile = p.k_order[w / p.H];
       const int h = static_cast<int>(w % p.H);
@@ -240,8 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = p.col_count[tile];
       if (n == 0) continue;
       const int32_t* list = p.col_list + static_cast<size_t>(tile) * nT;
-      bool ok = lane == 0 ? mbar_wait(&bar_kv_empty, (kv_it & 1) ^ 1, ctl, kSiteKvEmpty) : true;
-      if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
+      if (!wait1(&bar_kv_empty, (kv_it & 1) ^ 1, kSiteKvEmpty)) { alive = false; break; }
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar_kv_full, 2 * kTileBytes);
 #pragma unroll
@@ -250,29 +276,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(smem + S::kV + s * 16384, &tmap_v, &bar_kv_full, s * 64, h, kt * 128, b);
         }
       }
+      __syncwarp();
       ++kv_it;
-      const float* lse_row = p.lse + (static_cast<size_t>(b) * p.H + h) * p.L;
-      const float* delta_row = p.delta + (static_cast<size_t>(b) * p.H + h) * p.L;
-      for (int i = 0; i < n; ++i, ++qdo_it) {
+      for (int i = 0; i < n; ++i, ++qi) {
         const int qt = list[i];
-        ok = lane == 0 ? mbar_wait(&bar_qdo_empty, (qdo_it & 1) ^ 1, ctl, kSiteQdoEmpty) : true;
-        if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int c = lane * 4 + r;
-          const int qpos = qt * 128 + c;
-          const bool in = qpos < p.L;
-          lse2_s[c] = in ? lse_row[qpos] * kLog2e : -INFINITY;
-          delta_s[c] = in ? delta_row[qpos] : 0.0f;
-          qseq_s[c] = in ? p.seq_id[static_cast<size_t>(b) * p.L + qpos] : -1;
-        }
-        __syncwarp();
+        const int st = qi % kStages;
+        if (!wait1(&bar_qdo_empty[st], ((qi / kStages) & 1) ^ 1, kSiteQdoEmpty)) { alive = false; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_qdo_full, 2 * kTileBytes);
+          mbar_arrive_expect_tx(&bar_qdo_full[st], 2 * kTileBytes);
 #pragma unroll
           for (int s = 0; s < D / 64; ++s) {
-            tma_load_4d(smem + S::kQ + s * 16384, &tmap_q, &bar_qdo_full, s * 64, h, qt * 128, b);
-            tma_load_4d(smem + S::kDO + s * 16384, &tmap_do, &bar_qdo_full, s * 64, h, qt * 128, b);
+            tma_load_4d(smem + S::kQ + st * kTileBytes + s * 16384, &tmap_q, &bar_qdo_full[st], s * 64, h, qt * 128, b);
+            tma_load_4d(smem + S::kDO + st * kTileBytes + s * 16384, &tmap_do, &bar_qdo_full[st], s * 64, h, qt * 128,
+                        b);
           }
         }
         __syncwarp();
@@ -280,7 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (abort_s && lane == 0) {
       if (kv_it > 0) mbar_drain(&bar_kv_full, (kv_it - 1) & 1, 100000000ull);
-      if (qdo_it > 0) mbar_drain(&bar_qdo_full, (qdo_it - 1) & 1, 100000000ull);
+      for (uint32_t it = qi > kStages ? qi - kStages : 0; it <= qi; ++it)
+        mbar_drain(&bar_qdo_full[it % kStages], (it / kStages) & 1, 100000000ull);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -288,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_st = idesc_bf16(128, 128, false, false);  // S^T, dP^T
     constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);    // dV, dK
     constexpr uint32_t idesc_dq = idesc_bf16(128, D, true, true);      // dQ
-    uint32_t kv_it = 0, qdo_it = 0, item_it = 0;
+    uint32_t kv_it = 0, qi = 0, item_it = 0;
     bool alive = true;
     auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
       bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
@@ -300,8 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n == 0) continue;
       if (!wait1(&bar_kv_full, kv_it & 1, kSiteKvFull)) { alive = false; break; }
       ++kv_it;
-      for (int i = 0; i < n; ++i, ++qdo_it) {
-        if (!wait1(&bar_qdo_full, qdo_it & 1, kSiteQdoFull)) { alive = false; break; }
+      for (int i = 0; i < n; ++i, ++qi) {
+        const int st = qi % kStages;
+        const uint32_t sQ = sQ0 + st * kTileBytes;
+        const uint32_t sDO = sDO0 + st * kTileBytes;
+        if (!wait1(&bar_qdo_full[st], (qi / kStages) & 1, kSiteQdoFull)) { alive = false; break; }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
@@ -310,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&bar_s_full);
         }
         __syncwarp();
-        if (!wait1(&bar_dq_free, (qdo_it & 1) ^ 1, kSiteDqFree)) { alive = false; break; }
+        // dP^T overwrites the columns dQ of the previous query tile used
+        if (!wait1(&bar_dq_free, (qi & 1) ^ 1, kSiteDqFree)) { alive = false; break; }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
@@ -319,21 +340,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&bar_dp_full);
         }
         __syncwarp();
-        if (!wait1(&bar_ps_full, qdo_it & 1, kSitePsFull)) { alive = false; break; }
+        if (!wait1(&bar_ps_full, qi & 1, kSitePsFull)) { alive = false; break; }
         if (i == 0 && !wait1(&bar_acc_free, (item_it & 1) ^ 1, kSiteAccFree)) { alive = false; break; }
         tc_fence_after();
         if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(tmem + kColDV, kmajor_desc(sPT, kk), mnmajor_desc(sDO, kk), idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(tmem + kColDK, kmajor_desc(sDST, kk), mnmajor_desc(sQ, kk), idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          // dQ first, so its read-out overlaps the dV / dK MMAs
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_ss(tmem + kColDP, mnmajor_desc(sDST, kk), mnmajor_desc(sK, kk), idesc_dq, kk > 0 ? 1u : 0u);
+          umma_commit(&bar_dq_ready);
+          // dV += P^T dO_i with P^T in TMEM: query columns [0, 64) at TMEM
+          // columns [0, 32), [64, 128) at [64, 96)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + kColDV, tmem + kColS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmajor_desc(sDO, kk),
+                    idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(tmem + kColDK, kmajor_desc(sDST, kk), mnmajor_desc(sQ, kk), idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&bar_mma_done);
-          umma_commit(&bar_qdo_empty);
+          umma_commit(&bar_qdo_empty[st]);
         }
         __syncwarp();
       }
@@ -349,9 +375,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- compute
-    const int t = threadIdx.x;  // key row inside the tile == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t qdo_it = 0;
+    // Two warpgroups, g = 0 (warps 0-3) and g = 1 (warps 4-7).  Both cover the
+    // 128 key rows (thread row = TMEM lane); group g owns query columns
+    // [64 g, 64 g + 64) of S^T, dP^T, P^T, dS^T and feature columns
+    // [g D/2, (g + 1) D/2) of dQ, dK and dV, so the groups never exchange data.
+    constexpr int kHalfD = D / 2;
+    constexpr int kHalfChunks = kHalfD / 32;
+    const int g = warp >> 2;
+    const int row = threadIdx.x & 127;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t qi = 0, md_it = 0;
     bool alive = true;
     auto waitw = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
@@ -361,13 +394,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = static_cast<int>(w % p.H);
       const int b = tile / nT, kt = tile % nT;
       const int n = p.col_count[tile];
-      const int kpos = kt * 128 + t;
+      const int kpos = kt * 128 + row;
       const bool k_in = kpos < p.L;
-      const size_t krow = ((static_cast<size_t>(b) * p.L + kpos) * p.H + h) * D;
+      const size_t krow = ((static_cast<size_t>(b) * p.L + kpos) * p.H + h) * D + g * kHalfD;
       if (n == 0) {  // no valid key in this tile: zero gradients
         if (k_in) {
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
+          for (int c = 0; c < kHalfD / 8; ++c) {
             reinterpret_cast<uint4*>(p.dk + krow)[c] = make_uint4(0, 0, 0, 0);
             reinterpret_cast<uint4*>(p.dv + krow)[c] = make_uint4(0, 0, 0, 0);
           }
@@ -377,72 +410,94 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nfull = p.col_full[tile];
       const int32_t* list = p.col_list + static_cast<size_t>(tile) * nT;
       const int my_seq = k_in ? p.seq_id[static_cast<size_t>(b) * p.L + kpos] : -1;
-      for (int i = 0; i < n; ++i, ++qdo_it) {
+      const float* lse2_bh = p.lse2 + (static_cast<size_t>(b) * p.H + h) * p.Lp;
+      const float* delta_bh = p.delta + (static_cast<size_t>(b) * p.H + h) * p.Lp;
+      const int32_t* qseq_b = p.qseq + static_cast<size_t>(b) * p.Lp;
+      for (int i = 0; i < n; ++i, ++qi) {
         const int qt = list[i];
         const bool partial = i >= nfull;
-        if (!waitw(&bar_s_full, qdo_it & 1, kSiteSFull)) { alive = false; break; }
-        if (!waitw(&bar_dp_full, qdo_it & 1, kSiteDpFull)) { alive = false; break; }
-        if (!waitw(&bar_qdo_full, qdo_it & 1, kSiteQdoFullC)) { alive = false; break; }
+        const int q0 = qt * 128 + 64 * g;  // first query column of this group
+        const bool q_live = qseq_b[qt * 128 + row] >= 0;  // dQ row this thread adds
+        if (!waitw(&bar_s_full, qi & 1, kSiteSFull)) { alive = false; break; }
+        if (!waitw(&bar_dp_full, qi & 1, kSiteDpFull)) { alive = false; break; }
+        // dS^T of the previous query tile has been consumed: its dQ / dK MMAs
+        // were issued before this tile's dP^T, and MMAs complete in order
+        if (i > 0) {
+          if (!waitw(&bar_mma_done, md_it & 1, kSiteMmaDone)) { alive = false; break; }
+          ++md_it;
+        }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c2 = 0; c2 < 2; ++c2) {
           uint32_t rs[32], rd[32];
-          tmem_ld32(tmem + lane_base + kColS + c * 32, rs);
-          tmem_ld32(tmem + lane_base + kColDP + c * 32, rd);
+          tmem_ld32(tmem + lane_base + kColS + 64 * g + 32 * c2, rs);
+          tmem_ld32(tmem + lane_base + kColDP + 64 * g + 32 * c2, rd);
           tmem_wait_ld();
           uint32_t pp[16], dd[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float pv[2], dv[2];
+          for (int e4 = 0; e4 < 32; e4 += 4) {
+            const int q = q0 + 32 * c2 + e4;
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2_bh + q);
+            const float4 d4 = *reinterpret_cast<const float4*>(delta_bh + q);
+            int4 s4 = make_int4(my_seq, my_seq, my_seq, my_seq);
+            if (partial) s4 = *reinterpret_cast<const int4*>(qseq_b + q);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            const int sv[4] = {s4.x, s4.y, s4.z, s4.w};
+            float pv[4], dsv[4];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int q = c * 32 + e + u;
-              float pr = ex2(fmaf(__uint_as_float(rs[e + u]), p.scale_log2, -lse2_s[q]));
-              if (partial && (my_seq < 0 || qseq_s[q] != my_seq)) pr = 0.0f;
+            for (int u = 0; u < 4; ++u) {
+              float pr = ex2(fmaf(__uint_as_float(rs[e4 + u]), p.scale_log2, -lv[u]));
+              if (partial && (my_seq < 0 || sv[u] != my_seq)) pr = 0.0f;
               pv[u] = pr;
-              dv[u] = pr * (__uint_as_float(rd[e + u]) - delta_s[q]);
+              dsv[u] = pr * (__uint_as_float(rd[e4 + u]) - dv4[u]);
             }
-            pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
-            dd[e / 2] = pack_bf16x2(dv[0], dv[1]);
+            pp[e4 / 2] = pack_bf16x2(pv[0], pv[1]);
+            pp[e4 / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+            dd[e4 / 2] = pack_bf16x2(dsv[0], dsv[1]);
+            dd[e4 / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
           }
-          const uint32_t half = static_cast<uint32_t>(c >> 1) * 16384;
+          // P^T over S^T columns this group has already read; dS^T to shared memory
+          tmem_st16(tmem + lane_base + kColS + 64 * g + 16 * c2, pp);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint32_t off = half + sw128_offset(t, (c & 1) * 4 + v);
-            st_shared_v4(sPT + off, pp[4 * v], pp[4 * v + 1], pp[4 * v + 2], pp[4 * v + 3]);
+            const uint32_t off = static_cast<uint32_t>(g) * 16384 + sw128_offset(row, c2 * 4 + v);
             st_shared_v4(sDST + off, dd[4 * v], dd[4 * v + 1], dd[4 * v + 2], dd[4 * v + 3]);
           }
         }
-        const int qpos = qt * 128 + t;  // query row of dQ this thread adds
-        const bool q_live = qpos < p.L && qseq_s[t] >= 0;
+        tmem_wait_st();
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(&bar_ps_full);
-        if (!waitw(&bar_mma_done, qdo_it & 1, kSiteMmaDone)) { alive = false; break; }
+        if (!waitw(&bar_dq_ready, qi & 1, kSiteDqReady)) { alive = false; break; }
         tc_fence_after();
-        float* dqrow = p.dq_acc + ((static_cast<size_t>(b) * p.L + qpos) * p.H + h) * D;
+        uint32_t r[kHalfChunks][32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + kColDP + c * 32, r);
-          tmem_wait_ld();
-          if (q_live) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              red_add_v4(dqrow + c * 32 + v * 4, __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                         __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-          }
-        }
+        for (int c = 0; c < kHalfChunks; ++c) tmem_ld32(tmem + lane_base + kColDP + g * kHalfD + c * 32, r[c]);
+        tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar_dq_free);
+        if (q_live) {
+          const int qpos = qt * 128 + row;
+          float* dqrow = p.dq_acc + ((static_cast<size_t>(b) * p.L + qpos) * p.H + h) * D + g * kHalfD;
+#pragma unroll
+          for (int c = 0; c < kHalfChunks; ++c)
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              red_add_v4(dqrow + c * 32 + v * 4, __uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1]),
+                         __uint_as_float(r[c][4 * v + 2]), __uint_as_float(r[c][4 * v + 3]));
+        }
       }
       if (!alive) break;
-      // epilogue: the last mma_done covered every dV / dK MMA of this item
+      // epilogue: the last mma_done covers every dV / dK MMA of this item
+      if (!waitw(&bar_mma_done, md_it & 1, kSiteMmaDone)) { alive = false; break; }
+      ++md_it;
+      tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < kHalfChunks; ++c) {
         uint32_t rv[32], rk[32];
-        tmem_ld32(tmem + lane_base + kColDV + c * 32, rv);
-        tmem_ld32(tmem + lane_base + kColDK + c * 32, rk);
+        tmem_ld32(tmem + lane_base + kColDV + g * kHalfD + c * 32, rv);
+        tmem_ld32(tmem + lane_base + kColDK + g * kHalfD + c * 32, rk);
         tmem_wait_ld();
         if (k_in) {
 #pragma unroll
@@ -497,31 +552,38 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   const int sms = sm_count();
   if (!err || sms <= 0) return fail(PVL_ERR_CUDA, "masked_attn_bwd: no usable CUDA device");
 
-  float* dq_acc = static_cast<float*>(ws);
-  float* delta = reinterpret_cast<float*>(static_cast<char*>(ws) + bwd_ws_dq_bytes(B, L, H, D));
+  const int Lp = bwd_lp(L);
+  char* wsb = static_cast<char*>(ws);
+  float* dq_acc = reinterpret_cast<float*>(wsb);
+  float* delta = reinterpret_cast<float*>(wsb + bwd_ws_dq_bytes(B, L, H, D));
+  float* lse2 = reinterpret_cast<float*>(wsb + bwd_ws_dq_bytes(B, L, H, D) + bwd_ws_rows_bytes(B, L, H));
+  int32_t* qseq = reinterpret_cast<int32_t*>(wsb + bwd_ws_dq_bytes(B, L, H, D) + 2 * bwd_ws_rows_bytes(B, L, H));
   const long long rows = static_cast<long long>(B) * L * H;
 
   bwd_pre_kernel<D><<<grid_for(rows * (D / 8), 256), 256, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), delta, dq_acc, L, H, rows);
+      reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), lse, seq_id, delta, lse2,
+      qseq, dq_acc, B, L, Lp, H);
   st = check_cuda(cudaGetLastError(), "masked_attn_bwd preprocess launch");
   if (st != PVL_OK) return st;
 
   const TileMapView tm = tile_map_view(tile_ws, B, L, 128, 128, 0);
   BwdParams prm;
-  prm.seq_id = seq_id;
   prm.header = tm.header;
   prm.col_count = tm.col_count;
   prm.col_full = tm.col_full;
   prm.col_list = tm.col_list;
   prm.k_order = tm.k_order;
-  prm.lse = lse;
+  prm.seq_id = seq_id;
   prm.delta = delta;
+  prm.lse2 = lse2;
+  prm.qseq = qseq;
   prm.dq_acc = dq_acc;
   prm.dk = reinterpret_cast<__nv_bfloat16*>(dk);
   prm.dv = reinterpret_cast<__nv_bfloat16*>(dv);
   prm.err = err;
   prm.B = B;
   prm.L = L;
+  prm.Lp = Lp;
   prm.H = H;
   prm.nT = tm.nTk;
   prm.total_items = static_cast<long long>(B) * tm.nTk * H;
@@ -618,7 +680,7 @@ extern "C" pvl_status masked_attn_bwd_no_alloc(const pvl_bf16* q, const pvl_bf16
   if (need > kNoAllocScratchBytes)
     return fail(PVL_ERR_UNSUPPORTED,
                 "masked_attn_bwd_no_alloc: this shape needs %zu bytes of scratch; the library's static scratch "
-                "holds %zu bytes (B*L*H*(D+1)*4 must fit); use masked_attn_bwd with a workspace instead",
+                "holds %zu bytes (about B*L*H*(D+2)*4 must fit); use masked_attn_bwd with a workspace instead",
                 need, kNoAllocScratchBytes);
   void* scratch = nullptr;
   st = no_alloc_scratch(&scratch);

@@ -129,13 +129,20 @@ int sm_count();                                    // current device, 0 on failu
 // (INVALID_ARG), D, alignment and limits (UNSUPPORTED).
 pvl_status validate_attn(const char* who, const void* const* ptrs, int nptrs, int B, int L, int H, int D, float scale);
 
-// Bytes of the backward workspace: fp32 dQ accumulator [B, L, H, D] then
-// fp32 Delta [B, H, L], each 256-byte aligned.
+// Backward workspace, each part 256-byte aligned: the fp32 dQ accumulator
+// [B, L, H, D]; then, over query positions padded to whole 128-row tiles
+// (Lp), Delta and LSE * log2(e) as fp32 [B, H, Lp] and the query seq_ids as
+// int32 [B, Lp] (padding positions hold 0, 0 and -1).
+inline int bwd_lp(int L) { return ((L + 127) / 128) * 128; }
 inline size_t bwd_ws_dq_bytes(int B, int L, int H, int D) {
   return align256(static_cast<size_t>(B) * L * H * D * 4);
 }
+inline size_t bwd_ws_rows_bytes(int B, int L, int H) {
+  return align256(static_cast<size_t>(B) * H * bwd_lp(L) * 4);
+}
 inline size_t bwd_ws_total_bytes(int B, int L, int H, int D) {
-  return bwd_ws_dq_bytes(B, L, H, D) + align256(static_cast<size_t>(B) * H * L * 4);
+  return bwd_ws_dq_bytes(B, L, H, D) + 2 * bwd_ws_rows_bytes(B, L, H) +
+         align256(static_cast<size_t>(B) * bwd_lp(L) * 4);
 }
 
 // bf16 [B, L, H, D] tensor map with a (64 x 1 x 128 x 1) box and 128-byte
