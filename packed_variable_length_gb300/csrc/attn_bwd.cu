@@ -14,11 +14,14 @@
 //   bwd_main     one persistent CTA per SM over work items (b, key tile, head)
 //                in the tile map's longest-first key order.  Per item the K/V
 //                tile stays in shared memory while the non-empty query tiles
-//                stream through a 2-stage Q/dO ring (FULL first, PARTIAL last):
-//                  warp 8     TMA producer (K/V per item, Q_i and dO_i per tile);
+//                stream through (FULL first, PARTIAL last), Q in a 2-stage
+//                ring, dO with the tile's LSE / Delta / seq_id rows in one:
+//                  warp 8     TMA producer (K/V per item, Q_i, dO_i and the
+//                             row arrays per tile);
 //                  warp 9     TMEM owner and MMA issuer:
 //                             S^T = K Q_i^T, dP^T = V dO_i^T, then
-//                             dQ_i = dS K, dV += P^T dO_i, dK += dS^T Q_i;
+//                             dV += P^T dO_i (frees dO), dQ_i = dS K,
+//                             dK += dS^T Q_i;
 //                  warps 0-7  two warpgroups over the same 128 key rows
 //                             (thread row = TMEM lane), each owning half of
 //                             the query columns and half of the feature
@@ -27,10 +30,10 @@
 //                             tiles only); P^T goes back into TMEM over S^T
 //                             (the dV MMA reads it from there), dS^T into
 //                             swizzled shared memory (the dQ and dK MMAs read
-//                             it); then each adds half of its row of dQ_i
-//                             (TMEM lane = query row) into the accumulator
-//                             with vector reductions; at the end each writes
-//                             half of dK (times scale) and dV.
+//                             it); then each warp stages its 32 rows of
+//                             dQ_i in shared memory and adds them to the fp32
+//                             accumulator with TMA bulk reductions; at the
+//                             end each writes half of dK (times scale) and dV.
 //   bwd_convert  dQ = bf16(scale * accumulator).
 // The score matrix never reaches global memory.  Every wait is bounded.
 #include <cuda.h>
@@ -47,7 +50,7 @@ constexpr int kThreads = 320;  // warps 0-7 compute, 8 TMA, 9 MMA
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kComputeThreads = 256;
-constexpr int kStages = 2;        // Q/dO ring
+constexpr int kStages = 2;        // Q ring
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;     // S^T            [0, 128); P^T packed over [64 g, 64 g + 32)
 constexpr uint32_t kColDP = 128;  // dP^T, then dQ  [128, 256)
@@ -56,7 +59,7 @@ constexpr uint32_t kColDV = 256;  // dV             [256, 256 + D)
 
 enum BwdSite : uint32_t {
   kSiteKvEmpty = 21, kSiteQdoEmpty, kSiteKvFull, kSiteQdoFull, kSiteDqFree, kSitePsFull, kSiteAccFree,
-  kSiteSFull, kSiteDpFull, kSiteMmaDone, kSiteDqReady
+  kSiteSFull, kSiteDpFull, kSiteMmaDone, kSiteDqReady, kSiteDoEmpty, kSiteDoFull, kSiteDoFullC
 };
 
 template <int D>
@@ -64,10 +67,11 @@ struct BwdSmem {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
-  static constexpr int kQ = kV + kTile;            // kStages tiles
-  static constexpr int kDO = kQ + kStages * kTile;  // kStages tiles
-  static constexpr int kDST = kDO + kStages * kTile;  // dS^T bf16 [128 keys][128 queries]
-  static constexpr int kEnd = kDST + 128 * 256;
+  static constexpr int kQ = kV + kTile;             // kStages tiles
+  static constexpr int kDO = kQ + kStages * kTile;  // one tile
+  static constexpr int kDST = kDO + kTile;          // dS^T bf16 [128 keys][128 queries]
+  static constexpr int kStage = kDST + 128 * 256;   // dQ staging: 8 warps x 2 x (32 rows x 16 fp32)
+  static constexpr int kEnd = kStage + 8 * 4096;
   static constexpr int kBytes = (kEnd + 1024) > 120 * 1024 ? (kEnd + 1024) : 120 * 1024;
 };
 
@@ -186,13 +190,17 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p) {
   using S = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_qdo_full[kStages], bar_qdo_empty[kStages];
+  __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_q_full[kStages], bar_q_empty[kStages], bar_do_full, bar_do_empty;
   __shared__ uint64_t bar_s_full, bar_dp_full, bar_ps_full, bar_mma_done, bar_dq_ready, bar_dq_free, bar_acc_free,
       bar_final;
+  // LSE * log2(e), Delta and seq_id of the current query tile (loaded with dO)
+  __shared__ __align__(16) float lse2_s[128];
+  __shared__ __align__(16) float delta_s[128];
+  __shared__ __align__(16) int32_t qseq_s[128];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -216,9 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_kv_full, 1);
     mbar_init(&bar_kv_empty, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar_qdo_full[s], 1);
-      mbar_init(&bar_qdo_empty[s], 1);
+      mbar_init(&bar_q_full[s], 1);
+      mbar_init(&bar_q_empty[s], 1);
     }
+    mbar_init(&bar_do_full, 1);
+    mbar_init(&bar_do_empty, 1);
     mbar_init(&bar_s_full, 1);
     mbar_init(&bar_dp_full, 1);
     mbar_init(&bar_ps_full, kComputeThreads);
@@ -238,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_v);
     tma_prefetch_desc(&tmap_do);
+    tma_prefetch_desc(&tmap_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK = smem_u32(smem + S::kK);
   const uint32_t sV = smem_u32(smem + S::kV);
   const uint32_t sQ0 = smem_u32(smem + S::kQ);
-  const uint32_t sDO0 = smem_u32(smem + S::kDO);
+  const uint32_t sDO = smem_u32(smem + S::kDO);
   const uint32_t sDST = smem_u32(smem + S::kDST);
   constexpr uint32_t kTileBytes = S::kTile;
 
@@ -278,18 +289,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       ++kv_it;
+      const size_t row_off = (static_cast<size_t>(b) * p.H + h) * p.Lp;
       for (int i = 0; i < n; ++i, ++qi) {
         const int qt = list[i];
         const int st = qi % kStages;
-        if (!wait1(&bar_qdo_empty[st], ((qi / kStages) & 1) ^ 1, kSiteQdoEmpty)) { alive = false; break; }
+        if (!wait1(&bar_q_empty[st], ((qi / kStages) & 1) ^ 1, kSiteQdoEmpty)) { alive = false; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_qdo_full[st], 2 * kTileBytes);
+          mbar_arrive_expect_tx(&bar_q_full[st], kTileBytes);
 #pragma unroll
-          for (int s = 0; s < D / 64; ++s) {
-            tma_load_4d(smem + S::kQ + st * kTileBytes + s * 16384, &tmap_q, &bar_qdo_full[st], s * 64, h, qt * 128, b);
-            tma_load_4d(smem + S::kDO + st * kTileBytes + s * 16384, &tmap_do, &bar_qdo_full[st], s * 64, h, qt * 128,
-                        b);
-          }
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(smem + S::kQ + st * kTileBytes + s * 16384, &tmap_q, &bar_q_full[st], s * 64, h, qt * 128, b);
+        }
+        __syncwarp();
+        if (!wait1(&bar_do_empty, (qi & 1) ^ 1, kSiteDoEmpty)) { alive = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_do_full, kTileBytes + 3 * 512);
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(smem + S::kDO + s * 16384, &tmap_do, &bar_do_full, s * 64, h, qt * 128, b);
+          bulk_load(lse2_s, p.lse2 + row_off + qt * 128, 512, &bar_do_full);
+          bulk_load(delta_s, p.delta + row_off + qt * 128, 512, &bar_do_full);
+          bulk_load(qseq_s, p.qseq + static_cast<size_t>(b) * p.Lp + qt * 128, 512, &bar_do_full);
         }
         __syncwarp();
       }
@@ -297,7 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (abort_s && lane == 0) {
       if (kv_it > 0) mbar_drain(&bar_kv_full, (kv_it - 1) & 1, 100000000ull);
       for (uint32_t it = qi > kStages ? qi - kStages : 0; it <= qi; ++it)
-        mbar_drain(&bar_qdo_full[it % kStages], (it / kStages) & 1, 100000000ull);
+        mbar_drain(&bar_q_full[it % kStages], (it / kStages) & 1, 100000000ull);
+      if (qi > 0) mbar_drain(&bar_do_full, (qi - 1) & 1, 100000000ull);
+      mbar_drain(&bar_do_full, qi & 1, 100000000ull);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -320,8 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n; ++i, ++qi) {
         const int st = qi % kStages;
         const uint32_t sQ = sQ0 + st * kTileBytes;
-        const uint32_t sDO = sDO0 + st * kTileBytes;
-        if (!wait1(&bar_qdo_full[st], (qi / kStages) & 1, kSiteQdoFull)) { alive = false; break; }
+        if (!wait1(&bar_q_full[st], (qi / kStages) & 1, kSiteQdoFull)) { alive = false; break; }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
@@ -332,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         // dP^T overwrites the columns dQ of the previous query tile used
         if (!wait1(&bar_dq_free, (qi & 1) ^ 1, kSiteDqFree)) { alive = false; break; }
+        if (!wait1(&bar_do_full, qi & 1, kSiteDoFull)) { alive = false; break; }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
@@ -344,22 +366,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i == 0 && !wait1(&bar_acc_free, (item_it & 1) ^ 1, kSiteAccFree)) { alive = false; break; }
         tc_fence_after();
         if (lane == 0) {
-          // dQ first, so its read-out overlaps the dV / dK MMAs
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(tmem + kColDP, mnmajor_desc(sDST, kk), mnmajor_desc(sK, kk), idesc_dq, kk > 0 ? 1u : 0u);
-          umma_commit(&bar_dq_ready);
-          // dV += P^T dO_i with P^T in TMEM: query columns [0, 64) at TMEM
-          // columns [0, 32), [64, 128) at [64, 96)
+          // dV += P^T dO_i first (P^T in TMEM: query columns [0, 64) at TMEM
+          // columns [0, 32), [64, 128) at [64, 96)), so dO can be reloaded
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_ts(tmem + kColDV, tmem + kColS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmajor_desc(sDO, kk),
                     idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&bar_do_empty);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(tmem + kColDP, mnmajor_desc(sDST, kk), mnmajor_desc(sK, kk), idesc_dq, kk > 0 ? 1u : 0u);
+          umma_commit(&bar_dq_ready);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_ss(tmem + kColDK, kmajor_desc(sDST, kk), mnmajor_desc(sQ, kk), idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&bar_mma_done);
-          umma_commit(&bar_qdo_empty[st]);
+          umma_commit(&bar_q_empty[st]);
         }
         __syncwarp();
       }
@@ -381,10 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // [g D/2, (g + 1) D/2) of dQ, dK and dV, so the groups never exchange data.
     constexpr int kHalfD = D / 2;
     constexpr int kHalfChunks = kHalfD / 32;
+    constexpr int kRedChunks = kHalfD / 16;  // 16-float slices of dQ per TMA reduction
     const int g = warp >> 2;
     const int row = threadIdx.x & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t qi = 0, md_it = 0;
+    // per-warp dQ staging: two 32-row x 16-float buffers
+    uint8_t* stage = smem + S::kStage + warp * 4096;
+    uint32_t qi = 0, md_it = 0, red_it = 0;
     bool alive = true;
     auto waitw = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
@@ -410,16 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nfull = p.col_full[tile];
       const int32_t* list = p.col_list + static_cast<size_t>(tile) * nT;
       const int my_seq = k_in ? p.seq_id[static_cast<size_t>(b) * p.L + kpos] : -1;
-      const float* lse2_bh = p.lse2 + (static_cast<size_t>(b) * p.H + h) * p.Lp;
-      const float* delta_bh = p.delta + (static_cast<size_t>(b) * p.H + h) * p.Lp;
-      const int32_t* qseq_b = p.qseq + static_cast<size_t>(b) * p.Lp;
       for (int i = 0; i < n; ++i, ++qi) {
         const int qt = list[i];
         const bool partial = i >= nfull;
-        const int q0 = qt * 128 + 64 * g;  // first query column of this group
-        const bool q_live = qseq_b[qt * 128 + row] >= 0;  // dQ row this thread adds
         if (!waitw(&bar_s_full, qi & 1, kSiteSFull)) { alive = false; break; }
         if (!waitw(&bar_dp_full, qi & 1, kSiteDpFull)) { alive = false; break; }
+        // acquire this tile's LSE / Delta / seq_id rows (their phase can not
+        // advance before the dV MMA, which waits for this group)
+        if (!waitw(&bar_do_full, qi & 1, kSiteDoFullC)) { alive = false; break; }
         // dS^T of the previous query tile has been consumed: its dQ / dK MMAs
         // were issued before this tile's dP^T, and MMAs complete in order
         if (i > 0) {
@@ -436,11 +459,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pp[16], dd[16];
 #pragma unroll
           for (int e4 = 0; e4 < 32; e4 += 4) {
-            const int q = q0 + 32 * c2 + e4;
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2_bh + q);
-            const float4 d4 = *reinterpret_cast<const float4*>(delta_bh + q);
+            const int q = 64 * g + 32 * c2 + e4;
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2_s + q);
+            const float4 d4 = *reinterpret_cast<const float4*>(delta_s + q);
             int4 s4 = make_int4(my_seq, my_seq, my_seq, my_seq);
-            if (partial) s4 = *reinterpret_cast<const int4*>(qseq_b + q);
+            if (partial) s4 = *reinterpret_cast<const int4*>(qseq_s + q);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
             const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
             const int sv[4] = {s4.x, s4.y, s4.z, s4.w};
@@ -477,15 +500,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar_dq_free);
-        if (q_live) {
-          const int qpos = qt * 128 + row;
-          float* dqrow = p.dq_acc + ((static_cast<size_t>(b) * p.L + qpos) * p.H + h) * D + g * kHalfD;
+        // dQ_i rows of this warp (32 query rows) -> fp32 accumulator with TMA
+        // reductions of 32 x 16 slices; padding rows add exact zeros and rows
+        // past L are clipped by the tensor map.
 #pragma unroll
-          for (int c = 0; c < kHalfChunks; ++c)
+        for (int c = 0; c < kRedChunks; ++c) {
+          uint8_t* buf = stage + (red_it & 1) * 2048;
+          if (lane == 0) bulk_wait_group_read<1>();  // the reduction that last read this buffer is done reading
+          __syncwarp();
+          const uint32_t dst = smem_u32(buf + lane * 64);
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              red_add_v4(dqrow + c * 32 + v * 4, __uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1]),
-                         __uint_as_float(r[c][4 * v + 2]), __uint_as_float(r[c][4 * v + 3]));
+          for (int v = 0; v < 4; ++v)
+            st_shared_v4(dst + v * 16, r[c >> 1][(c & 1) * 16 + 4 * v], r[c >> 1][(c & 1) * 16 + 4 * v + 1],
+                         r[c >> 1][(c & 1) * 16 + 4 * v + 2], r[c >> 1][(c & 1) * 16 + 4 * v + 3]);
+          fence_async_smem();
+          __syncwarp();
+          const int row0 = qt * 128 + (warp & 3) * 32;
+          if (lane == 0 && row0 < p.L) {  // a box wholly past L is skipped, not issued
+            tma_reduce_add_4d(&tmap_dq, buf, g * kHalfD + 16 * c, h, row0, b);
+            bulk_commit_group();
+          }
+          ++red_it;
         }
       }
       if (!alive) break;
@@ -519,6 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bar_acc_free);
     }
+    // every dQ reduction of this warp has completed before the CTA leaves
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -542,7 +580,7 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
                       const pvl_bf16* dO, const float* lse, const int32_t* seq_id, const void* tile_ws, int B,
                       int L, int H, float scale, pvl_bf16* dq, pvl_bf16* dk, pvl_bf16* dv, void* ws,
                       cudaStream_t stream) {
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   pvl_status st = make_bhld_tensor_map(&tq, q, B, L, H, D);
   if (st == PVL_OK) st = make_bhld_tensor_map(&tk, k, B, L, H, D);
   if (st == PVL_OK) st = make_bhld_tensor_map(&tv, v, B, L, H, D);
@@ -551,6 +589,8 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   DeviceError* err = device_error_record();
   const int sms = sm_count();
   if (!err || sms <= 0) return fail(PVL_ERR_CUDA, "masked_attn_bwd: no usable CUDA device");
+  st = make_bhld_f32_tensor_map(&tdq, ws, B, L, H, D, 16, 32);  // dQ accumulator at the start of ws
+  if (st != PVL_OK) return st;
 
   const int Lp = bwd_lp(L);
   char* wsb = static_cast<char*>(ws);
@@ -595,7 +635,7 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
                   "masked_attn_bwd smem attribute");
   if (st != PVL_OK) return st;
   const long long grid = prm.total_items < sms ? prm.total_items : sms;
-  bwd_main_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tq, tk, tv, tdo, prm);
+  bwd_main_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, prm);
   st = check_cuda(cudaGetLastError(), "masked_attn_bwd main launch");
   if (st != PVL_OK) return st;
 

@@ -89,7 +89,25 @@ pvl_status validate_attn(const char* who, const void* const* ptrs, int nptrs, in
   return PVL_OK;
 }
 
+namespace {
+pvl_status encode_bhld(void* map_out, const void* base, CUtensorMapDataType type, int esize, int B, int L, int H,
+                       int D, const cuuint32_t box[4], CUtensorMapSwizzle swizzle);
+}  // namespace
+
 pvl_status make_bhld_tensor_map(void* map_out, const void* base, int B, int L, int H, int D) {
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  return encode_bhld(map_out, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, L, H, D, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+pvl_status make_bhld_f32_tensor_map(void* map_out, const void* base, int B, int L, int H, int D, int box_d,
+                                    int box_rows) {
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_d), 1, static_cast<cuuint32_t>(box_rows), 1};
+  return encode_bhld(map_out, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, L, H, D, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+namespace {
+pvl_status encode_bhld(void* map_out, const void* base, CUtensorMapDataType type, int esize, int B, int L, int H,
+                       int D, const cuuint32_t box[4], CUtensorMapSwizzle swizzle) {
   // cuTensorMapEncodeTiled is a driver call and needs a current context on
   // this thread.  A thread that has made no runtime call yet (for example a
   // torch autograd worker) has none; setting the current device binds the
@@ -114,17 +132,17 @@ pvl_status make_bhld_tensor_map(void* map_out, const void* base, int B, int L, i
   }
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
-                                 static_cast<cuuint64_t>(L) * H * D * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint64_t es = static_cast<cuuint64_t>(esize);
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * es, static_cast<cuuint64_t>(H) * D * es,
+                                 static_cast<cuuint64_t>(L) * H * D * es};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = g_encode(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(map_out), type, 4, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PVL_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
   return PVL_OK;
 }
+}  // namespace
 
 }  // namespace pvl
 
