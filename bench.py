@@ -38,6 +38,8 @@ sys.path.insert(0, ROOT)
 METRIC = "effective masked-attn fwd+bwd TFLOP/s and tokens/s at 1 GB300; % of bf16 peak"
 FLOPS_PER_PAIR_FWD = 4
 FLOPS_PER_PAIR_BWD = 10
+# kernels per step: seq_ids 1, tile map 3 per level x 2 levels, forward 1, backward 3
+LAUNCHES_PER_STEP = 11
 
 
 def load_peaks():
@@ -317,7 +319,7 @@ def run_gpu(args):
         "clocks": clk,
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 8 * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "roofline": {
             "kernel": "masked_attn_bwd (bwd_pre + bwd_main + bwd_convert launches, timed together)",
             "bound": "tensor", "achieved": round(bwd_achieved, 2), "peak": peak, "unit": "TFLOP/s",

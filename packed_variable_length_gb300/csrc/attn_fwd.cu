@@ -10,7 +10,8 @@
 // Design.  One persistent CTA per SM walks work items (b, query-tile pair,
 // head): two adjacent 128-row query tiles A and B that share one stream of
 // key tiles, taken from level 1 of the tile map (256-row query tiles) in its
-// longest-first order, round-robin over CTAs.  Only the key tiles the map
+// longest-first order with heads innermost (the CTAs running together read
+// the adjacent per-head slices of the same token rows), round-robin over CTAs.  Only the key tiles the map
 // lists as non-empty are touched, FULL ones first (no per-element mask),
 // then PARTIAL ones (mask from the seq_ids).
 //   warp 8      TMA producer: the Q pair once per item, K and V tiles into
@@ -77,7 +78,7 @@ struct FwdParams {
   float* lse;
   DeviceError* err;
   int B, L, H, nP, nK;       // query-tile pairs and key tiles per row
-  long long total_items;
+  long long total_items;  // tiles * H, heads innermost
   float scale_log2;
   uint64_t timeout_ns;
 };
