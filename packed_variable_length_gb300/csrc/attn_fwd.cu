@@ -121,6 +121,63 @@ __device__ __forceinline__ uint32_t key_mask_word(const int32_t* __restrict__ se
   return bits;
 }
 
+// Row max of one 128-key S row in TMEM (four 32-column loads).  kMasked:
+// PARTIAL tile, inadmissible keys excluded.
+template <bool kMasked>
+__device__ __forceinline__ float row_max(uint32_t s_col, const int32_t* seq_row, int L, int kt, int my_seq) {
+  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    tmem_ld32(s_col + 32 * c, r);
+    const uint32_t mk = kMasked ? key_mask_word(seq_row, L, kt, c, my_seq) : ~0u;
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float v = __uint_as_float(r[i]);
+      mx4[i & 3] = fmaxf(mx4[i & 3], kMasked ? ((mk >> i) & 1u ? v : -INFINITY) : v);
+    }
+  }
+  return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+}
+
+// P = 2^(scale_log2 * S + neg_m) for one row, written as packed bf16 over the
+// first 64 columns of the same S buffer (each 32-column chunk is read before
+// the 16 columns it overwrites); returns the row sum of P.
+template <bool kMasked>
+__device__ __forceinline__ float exp_store(uint32_t s_col, const int32_t* seq_row, int L, int kt, int my_seq,
+                                           bool any, float scale_log2, float neg_m) {
+  const float2 c2 = make_float2(scale_log2, scale_log2);
+  const float2 m2 = make_float2(neg_m, neg_m);
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    tmem_ld32(s_col + 32 * c, r);
+    uint32_t mk = ~0u;
+    if (kMasked) {
+      mk = any ? key_mask_word(seq_row, L, kt, c, my_seq) : 0u;
+      asm volatile("" : "+r"(mk));  // recomputed here rather than kept live from pass 1
+    }
+    tmem_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const float2 x = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, m2);
+      float p0 = ex2(x.x), p1 = ex2(x.y);
+      if (kMasked) {
+        p0 = (mk >> e) & 1u ? p0 : 0.0f;
+        p1 = (mk >> (e + 1)) & 1u ? p1 : 0.0f;
+      }
+      if ((e >> 1) & 1) acc1 = fadd2(acc1, make_float2(p0, p1));
+      else acc0 = fadd2(acc0, make_float2(p0, p1));
+      pk[e >> 1] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16(s_col + 16 * c, pk);
+  }
+  return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -373,46 +430,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!waitw(&bar_s_full[x], s_it & 1, kSiteSFull)) { alive = false; break; }
         ++s_it;
         tc_fence_after();
-        // pass 1: row max
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(s_col + 32 * c, r);
-          const uint32_t mk = partial ? key_mask_word(seq_row, p.L, kt, c, my_seq) : ~0u;
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            mx4[i & 3] = fmaxf(mx4[i & 3], (mk >> i) & 1u ? __uint_as_float(r[i]) : -INFINITY);
-        }
-        const float mx2 = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+        // pass 1: row max (FULL tiles need no mask)
+        float mx;
+        if (!partial) mx = row_max<false>(s_col, seq_row, p.L, kt, my_seq);
+        else mx = row_max<true>(s_col, seq_row, p.L, kt, my_seq);
+        const float mx2 = mx * p.scale_log2;
         const bool grow = mx2 > m_ref + kRescaleThreshold;
         const float m_new = grow ? mx2 : m_ref;
         const float alpha = grow ? ex2(m_ref - m_new) : 1.0f;
         const bool any = m_new != -INFINITY;
         const float neg_m = any ? -m_new : 0.0f;
         // pass 2: P = 2^(scale*log2e*S - m), packed bf16 over S columns [0, 64)
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(s_col + 32 * c, r);
-          uint32_t mk = !any ? 0u : partial ? key_mask_word(seq_row, p.L, kt, c, my_seq) : ~0u;
-          asm volatile("" : "+r"(mk));  // recomputed here rather than kept live from pass 1
-          tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const bool k0 = (mk >> e) & 1u;
-            const bool k1 = (mk >> (e + 1)) & 1u;
-            const float p0 = k0 ? ex2(fmaf(__uint_as_float(r[e]), p.scale_log2, neg_m)) : 0.0f;
-            const float p1 = k1 ? ex2(fmaf(__uint_as_float(r[e + 1]), p.scale_log2, neg_m)) : 0.0f;
-            l4[(e >> 1) & 3] += p0 + p1;
-            pk[e >> 1] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(s_col + 16 * c, pk);
-        }
-        l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+        float lsum;
+        if (!partial) lsum = exp_store<false>(s_col, seq_row, p.L, kt, my_seq, any, p.scale_log2, neg_m);
+        else lsum = exp_store<true>(s_col, seq_row, p.L, kt, my_seq, any, p.scale_log2, neg_m);
+        l = l * alpha + lsum;
         // PV_x of the previous key tile has completed (S_x of this tile was
         // issued after it); rescale O_x when the max grew.
         if (j > 0) {
