@@ -185,6 +185,52 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restric
   }
 }
 
+// P^T and dS^T for the 64 query columns of group g of one key row: reads
+// S^T and dP^T from TMEM, LSE*log2e / Delta / seq_id from shared memory,
+// writes P^T (packed bf16) back over S^T columns this group has read and
+// dS^T (bf16) into the swizzled shared tile.  kMasked: PARTIAL tile.
+template <bool kMasked>
+__device__ __forceinline__ void pds_chunks(uint32_t tmem_lane, int g, int row, uint32_t sDST, const float* lse2_s,
+                                           const float* delta_s, const int32_t* qseq_s, int my_seq, float scale_log2) {
+  const float2 c2 = make_float2(scale_log2, scale_log2);
+#pragma unroll 1
+  for (int c2i = 0; c2i < 2; ++c2i) {
+    uint32_t rs[32], rd[32];
+    tmem_ld32(tmem_lane + kColS + 64 * g + 32 * c2i, rs);
+    tmem_ld32(tmem_lane + kColDP + 64 * g + 32 * c2i, rd);
+    tmem_wait_ld();
+    uint32_t pp[16], dd[16];
+#pragma unroll
+    for (int e4 = 0; e4 < 32; e4 += 4) {
+      const int q = 64 * g + 32 * c2i + e4;
+      const float4 l4 = *reinterpret_cast<const float4*>(lse2_s + q);
+      const float4 d4 = *reinterpret_cast<const float4*>(delta_s + q);
+#pragma unroll
+      for (int u = 0; u < 4; u += 2) {
+        const float2 lv = u == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w);
+        const float2 dv = u == 0 ? make_float2(-d4.x, -d4.y) : make_float2(-d4.z, -d4.w);
+        const float2 x = ffma2(make_float2(__uint_as_float(rs[e4 + u]), __uint_as_float(rs[e4 + u + 1])), c2, lv);
+        float2 pv = make_float2(ex2(x.x), ex2(x.y));
+        if (kMasked) {
+          const int4 s4 = *reinterpret_cast<const int4*>(qseq_s + q);
+          const int sa = u == 0 ? s4.x : s4.z, sb = u == 0 ? s4.y : s4.w;
+          if (my_seq < 0 || sa != my_seq) pv.x = 0.0f;
+          if (my_seq < 0 || sb != my_seq) pv.y = 0.0f;
+        }
+        const float2 ds = fmul2(pv, fadd2(make_float2(__uint_as_float(rd[e4 + u]), __uint_as_float(rd[e4 + u + 1])), dv));
+        pp[(e4 + u) / 2] = pack_bf16x2(pv.x, pv.y);
+        dd[(e4 + u) / 2] = pack_bf16x2(ds.x, ds.y);
+      }
+    }
+    tmem_st16(tmem_lane + kColS + 64 * g + 16 * c2i, pp);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint32_t off = static_cast<uint32_t>(g) * 16384 + sw128_offset(row, c2i * 4 + v);
+      st_shared_v4(sDST + off, dd[4 * v], dd[4 * v + 1], dd[4 * v + 2], dd[4 * v + 3]);
+    }
+  }
+}
+
 // --------------------------------------------------------------------- main
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -450,44 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++md_it;
         }
         tc_fence_after();
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t rs[32], rd[32];
-          tmem_ld32(tmem + lane_base + kColS + 64 * g + 32 * c2, rs);
-          tmem_ld32(tmem + lane_base + kColDP + 64 * g + 32 * c2, rd);
-          tmem_wait_ld();
-          uint32_t pp[16], dd[16];
-#pragma unroll
-          for (int e4 = 0; e4 < 32; e4 += 4) {
-            const int q = 64 * g + 32 * c2 + e4;
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2_s + q);
-            const float4 d4 = *reinterpret_cast<const float4*>(delta_s + q);
-            int4 s4 = make_int4(my_seq, my_seq, my_seq, my_seq);
-            if (partial) s4 = *reinterpret_cast<const int4*>(qseq_s + q);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            const int sv[4] = {s4.x, s4.y, s4.z, s4.w};
-            float pv[4], dsv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float pr = ex2(fmaf(__uint_as_float(rs[e4 + u]), p.scale_log2, -lv[u]));
-              if (partial && (my_seq < 0 || sv[u] != my_seq)) pr = 0.0f;
-              pv[u] = pr;
-              dsv[u] = pr * (__uint_as_float(rd[e4 + u]) - dv4[u]);
-            }
-            pp[e4 / 2] = pack_bf16x2(pv[0], pv[1]);
-            pp[e4 / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-            dd[e4 / 2] = pack_bf16x2(dsv[0], dsv[1]);
-            dd[e4 / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
-          }
-          // P^T over S^T columns this group has already read; dS^T to shared memory
-          tmem_st16(tmem + lane_base + kColS + 64 * g + 16 * c2, pp);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint32_t off = static_cast<uint32_t>(g) * 16384 + sw128_offset(row, c2 * 4 + v);
-            st_shared_v4(sDST + off, dd[4 * v], dd[4 * v + 1], dd[4 * v + 2], dd[4 * v + 3]);
-          }
-        }
+        if (!partial)
+          pds_chunks<false>(tmem + lane_base, g, row, sDST, lse2_s, delta_s, qseq_s, my_seq, p.scale_log2);
+        else
+          pds_chunks<true>(tmem + lane_base, g, row, sDST, lse2_s, delta_s, qseq_s, my_seq, p.scale_log2);
         tmem_wait_st();
         fence_async_smem();
         tc_fence_before();
