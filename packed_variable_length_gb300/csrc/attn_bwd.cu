@@ -70,7 +70,7 @@ struct BwdSmem {
   static constexpr int kQ = kV + kTile;             // kStages tiles
   static constexpr int kDO = kQ + kStages * kTile;  // one tile
   static constexpr int kDST = kDO + kTile;          // dS^T bf16 [128 keys][128 queries]
-  static constexpr int kStage = kDST + 128 * 256;   // dQ staging: 8 warps x 2 x (32 rows x 16 fp32)
+  static constexpr int kStage = kDST + 128 * 256;   // dQ staging: 8 warps x (32 rows x 32 fp32)
   static constexpr int kEnd = kStage + 8 * 4096;
   static constexpr int kBytes = (kEnd + 1024) > 120 * 1024 ? (kEnd + 1024) : 120 * 1024;
 };
@@ -449,13 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // [g D/2, (g + 1) D/2) of dQ, dK and dV, so the groups never exchange data.
     constexpr int kHalfD = D / 2;
     constexpr int kHalfChunks = kHalfD / 32;
-    constexpr int kRedChunks = kHalfD / 16;  // 16-float slices of dQ per TMA reduction
     const int g = warp >> 2;
     const int row = threadIdx.x & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // per-warp dQ staging: two 32-row x 16-float buffers
+    // per-warp dQ staging: one 32-row x 32-float buffer (slice 0)
     uint8_t* stage = smem + S::kStage + warp * 4096;
-    uint32_t qi = 0, md_it = 0, red_it = 0;
+    uint32_t qi = 0, md_it = 0;
     bool alive = true;
     auto waitw = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
@@ -489,12 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // acquire this tile's LSE / Delta / seq_id rows (their phase can not
         // advance before the dV MMA, which waits for this group)
         if (!waitw(&bar_do_full, qi & 1, kSiteDoFullC)) { alive = false; break; }
-        // dS^T of the previous query tile has been consumed: its dQ / dK MMAs
-        // were issued before this tile's dP^T, and MMAs complete in order
-        if (i > 0) {
-          if (!waitw(&bar_mma_done, md_it & 1, kSiteMmaDone)) { alive = false; break; }
-          ++md_it;
-        }
+        // this warp's dS^T slice held two dQ chunks of the previous tile: their
+        // reductions must have finished reading it
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
         tc_fence_after();
         if (!partial)
           pds_chunks<false>(tmem + lane_base, g, row, sDST, lse2_s, delta_s, qseq_s, my_seq, p.scale_log2);
@@ -512,33 +509,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar_dq_free);
-        // dQ_i rows of this warp (32 query rows) -> fp32 accumulator with TMA
-        // reductions of 32 x 16 slices; padding rows add exact zeros and rows
-        // past L are clipped by the tensor map.
+        // dQ_i rows of this warp (32 query rows x this group's D/2 columns) ->
+        // fp32 accumulator with TMA reductions of 32 x 32 slices.  Slice 0 goes
+        // through the warp's staging buffer, slice 1 (D = 128) through the
+        // warp's own 4 KB of the dS^T tile once the dQ / dK MMAs are done with
+        // it; padding rows add exact zeros, boxes wholly past L are skipped.
+        const int row0 = qt * 128 + (warp & 3) * 32;
+        uint8_t* dst_slice = smem + S::kDST + g * 16384 + (warp & 3) * 4096;
 #pragma unroll
-        for (int c = 0; c < kRedChunks; ++c) {
-          uint8_t* buf = stage + (red_it & 1) * 2048;
-          if (lane == 0) bulk_wait_group_read<1>();  // the reduction that last read this buffer is done reading
-          __syncwarp();
-          const uint32_t dst = smem_u32(buf + lane * 64);
+        for (int c = 0; c < kHalfChunks; ++c) {
+          if (c == 1) {
+            if (!waitw(&bar_mma_done, md_it & 1, kSiteMmaDone)) { alive = false; break; }
+            ++md_it;
+          }
+          uint8_t* buf = c == 0 ? stage : dst_slice;
+          // 128-byte swizzle (the map's): 16-byte chunk v of row `lane` sits at
+          // chunk v ^ (lane & 7), so the eight lanes of a store phase hit
+          // distinct banks
+          const uint32_t dst = smem_u32(buf + lane * 128);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            st_shared_v4(dst + v * 16, r[c >> 1][(c & 1) * 16 + 4 * v], r[c >> 1][(c & 1) * 16 + 4 * v + 1],
-                         r[c >> 1][(c & 1) * 16 + 4 * v + 2], r[c >> 1][(c & 1) * 16 + 4 * v + 3]);
+          for (int v = 0; v < 8; ++v)
+            st_shared_v4(dst + ((v ^ (lane & 7)) << 4), r[c][4 * v], r[c][4 * v + 1], r[c][4 * v + 2],
+                         r[c][4 * v + 3]);
           fence_async_smem();
           __syncwarp();
-          const int row0 = qt * 128 + (warp & 3) * 32;
-          if (lane == 0 && row0 < p.L) {  // a box wholly past L is skipped, not issued
-            tma_reduce_add_4d(&tmap_dq, buf, g * kHalfD + 16 * c, h, row0, b);
-            bulk_commit_group();
-          }
-          ++red_it;
+          if (lane == 0 && row0 < p.L) tma_reduce_add_4d(&tmap_dq, buf, g * kHalfD + 32 * c, h, row0, b);
         }
+        if (!alive) break;
+        if (kHalfChunks < 2) {  // D = 64: the dS^T slice was not used, but the MMAs must still be waited for
+          if (!waitw(&bar_mma_done, md_it & 1, kSiteMmaDone)) { alive = false; break; }
+          ++md_it;
+        }
+        if (lane == 0) bulk_commit_group();
       }
       if (!alive) break;
-      // epilogue: the last mma_done covers every dV / dK MMA of this item
-      if (!waitw(&bar_mma_done, md_it & 1, kSiteMmaDone)) { alive = false; break; }
-      ++md_it;
+      // epilogue: the last tile's mma_done (waited above) covers every dV / dK
+      // MMA of this item
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < kHalfChunks; ++c) {
@@ -601,7 +607,7 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   DeviceError* err = device_error_record();
   const int sms = sm_count();
   if (!err || sms <= 0) return fail(PVL_ERR_CUDA, "masked_attn_bwd: no usable CUDA device");
-  st = make_bhld_f32_tensor_map(&tdq, ws, B, L, H, D, 16, 32);  // dQ accumulator at the start of ws
+  st = make_bhld_f32_tensor_map(&tdq, ws, B, L, H, D, 32, 32);  // dQ accumulator at the start of ws
   if (st != PVL_OK) return st;
 
   const int Lp = bwd_lp(L);

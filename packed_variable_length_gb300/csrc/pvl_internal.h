@@ -150,8 +150,9 @@ inline size_t bwd_ws_total_bytes(int B, int L, int H, int D) {
 pvl_status make_bhld_tensor_map(void* map_out /* CUtensorMap* */, const void* base, int B, int L, int H,
                                 int D);
 
-// fp32 [B, L, H, D] tensor map with a (box_d x 1 x box_rows x 1) box and no
-// swizzle (rows of box_d floats, packed), for TMA reductions.
+// fp32 [B, L, H, D] tensor map with a (box_d x 1 x box_rows x 1) box, for TMA
+// reductions.  A 128-byte box row (box_d = 32) takes the 128-byte swizzle; a
+// narrower one none (rows of box_d floats, packed).
 pvl_status make_bhld_f32_tensor_map(void* map_out /* CUtensorMap* */, const void* base, int B, int L, int H, int D,
                                     int box_d, int box_rows);
 

@@ -102,7 +102,10 @@ pvl_status make_bhld_tensor_map(void* map_out, const void* base, int B, int L, i
 pvl_status make_bhld_f32_tensor_map(void* map_out, const void* base, int B, int L, int H, int D, int box_d,
                                     int box_rows) {
   const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_d), 1, static_cast<cuuint32_t>(box_rows), 1};
-  return encode_bhld(map_out, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, L, H, D, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  // a 128-byte box row takes the 128-byte swizzle, so that a warp writing one
+  // row per lane stages it without shared-memory bank conflicts
+  const CUtensorMapSwizzle sw = box_d * 4 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return encode_bhld(map_out, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, L, H, D, box, sw);
 }
 
 namespace {
