@@ -23,11 +23,12 @@
 //               so the tensor core works on one query tile while the other
 //               tile's softmax runs.  PV reads P straight from TMEM.
 //   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: thread t owns
-//               query row t (TMEM lane t).  Pass 1 takes the row max of S;
-//               pass 2 re-reads S, applies the mask (PARTIAL tiles only),
-//               computes P = exp2(scale*log2e*S - m), accumulates the row
-//               sum and writes P as packed bf16 over the first 64 columns of
-//               the same S buffer.  O is rescaled in TMEM only when the
+//               query row t (TMEM lane t).  The whole 128-key row of S comes
+//               into registers with one TMEM wait (warpgroup 2 gives up
+//               registers for this); in PARTIAL tiles inadmissible keys are
+//               set to -inf.  Then the row max, P = exp2(scale*log2e*S - m)
+//               with its row sum, and P written as packed bf16 over the first
+//               64 columns of the same S buffer.  O is rescaled in TMEM only when the
 //               running max grows by more than 2^8 (the stale max bounds
 //               every P by 256 and the final division uses the same max).
 //               The epilogue divides by the row sum and writes O and LSE.
@@ -41,7 +42,13 @@
 namespace pvl {
 namespace {
 
-constexpr int kThreads = 320;  // warps 0-7 softmax (two groups), 8 TMA, 9 MMA
+// warps 0-7 softmax (two warpgroups), 8 TMA, 9 MMA, 10-11 idle: they complete
+// the third warpgroup, whose registers go to the softmax groups
+constexpr int kThreads = 384;
+// registers per thread after reallocation: 256 x 208 + 128 x 88 = 384 x 168,
+// the launch's own allotment (168 = 65536 / 384 rounded down to 8)
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsOther = 88;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kStages = 2;
@@ -121,54 +128,58 @@ __device__ __forceinline__ uint32_t key_mask_word(const int32_t* __restrict__ se
   return bits;
 }
 
-// Row max of one 128-key S row in TMEM (four 32-column loads).  kMasked:
-// PARTIAL tile, inadmissible keys excluded.
-template <bool kMasked>
-__device__ __forceinline__ float row_max(uint32_t s_col, const int32_t* seq_row, int L, int kt, int my_seq) {
-  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    uint32_t r[32];
-    tmem_ld32(s_col + 32 * c, r);
-    const uint32_t mk = kMasked ? key_mask_word(seq_row, L, kt, c, my_seq) : ~0u;
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float v = __uint_as_float(r[i]);
-      mx4[i & 3] = fmaxf(mx4[i & 3], kMasked ? ((mk >> i) & 1u ? v : -INFINITY) : v);
-    }
-  }
-  return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
-// P = 2^(scale_log2 * S + neg_m) for one row, written as packed bf16 over the
-// first 64 columns of the same S buffer (each 32-column chunk is read before
-// the 16 columns it overwrites); returns the row sum of P.
+// One query row of S (128 keys) into registers with a single TMEM wait; in a
+// PARTIAL tile the inadmissible keys are set to -inf, so that they drop out
+// of the max and exponentiate to 0.  Returns the row max of S.
 template <bool kMasked>
-__device__ __forceinline__ float exp_store(uint32_t s_col, const int32_t* seq_row, int L, int kt, int my_seq,
-                                           bool any, float scale_log2, float neg_m) {
+__device__ __forceinline__ float load_row(uint32_t s_col, uint32_t (&s)[4][32], const int32_t* seq_row, int L, int kt,
+                                          int my_seq) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld32(s_col + 32 * c, s[c]);
+  uint32_t mk[4];
+  if (kMasked) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) mk[c] = key_mask_word(seq_row, L, kt, c, my_seq);
+  }
+  tmem_wait_ld();
+  if (kMasked) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (!((mk[c] >> i) & 1u)) s[c][i] = __float_as_uint(-INFINITY);
+  }
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int i = 0; i < 32; i += 8)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        m[u] = fmax3(m[u], __uint_as_float(s[c][i + 2 * u]), __uint_as_float(s[c][i + 2 * u + 1]));
+  return fmax3(m[0], m[1], fmaxf(m[2], m[3]));
+}
+
+// P = 2^(scale_log2 * S + neg_m) for one row held in registers, written as
+// packed bf16 over the first 64 columns of the same S buffer; returns the row
+// sum of P.  Masked keys hold -inf and give exactly 0.
+__device__ __forceinline__ float exp_store(uint32_t s_col, const uint32_t (&s)[4][32], float scale_log2, float neg_m) {
   const float2 c2 = make_float2(scale_log2, scale_log2);
   const float2 m2 = make_float2(neg_m, neg_m);
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll 1
+#pragma unroll
   for (int c = 0; c < 4; ++c) {
-    uint32_t r[32];
-    tmem_ld32(s_col + 32 * c, r);
-    uint32_t mk = ~0u;
-    if (kMasked) {
-      mk = any ? key_mask_word(seq_row, L, kt, c, my_seq) : 0u;
-      asm volatile("" : "+r"(mk));  // recomputed here rather than kept live from pass 1
-    }
-    tmem_wait_ld();
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-      const float2 x = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, m2);
-      float p0 = ex2(x.x), p1 = ex2(x.y);
-      if (kMasked) {
-        p0 = (mk >> e) & 1u ? p0 : 0.0f;
-        p1 = (mk >> (e + 1)) & 1u ? p1 : 0.0f;
-      }
+      const float2 x = ffma2(make_float2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), c2, m2);
+      const float p0 = ex2(x.x), p1 = ex2(x.y);
       if ((e >> 1) & 1) acc1 = fadd2(acc1, make_float2(p0, p1));
       else acc0 = fadd2(acc0, make_float2(p0, p1));
       pk[e >> 1] = pack_bf16x2(p0, p1);
@@ -245,152 +256,159 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sV0 = smem_u32(smem + S::kV);
   constexpr uint32_t kTileBytes = S::kTile;
 
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------------------ producer
-    uint32_t kv_it = 0, q_it = 0;
-    bool alive = true;
-    auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
-      bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
-      return __shfl_sync(0xffffffffu, ok, 0);
-    };
-    for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
-      const int tile = p.q_order[w / p.H];
-      const int h = static_cast<int>(w % p.H);
-      const int b = tile / nP, pp = tile % nP;
-      const int n = p.row_count[tile];
-      if (n == 0) continue;
-      const int32_t* list = p.row_list + static_cast<size_t>(tile) * nK;
-      if (!wait1(&bar_q_empty, (q_it & 1) ^ 1, kSiteQEmpty)) { alive = false; break; }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_q_full, 2 * kTileBytes);
-#pragma unroll
-        for (int x = 0; x < 2; ++x)
-#pragma unroll
-          for (int s = 0; s < D / 64; ++s)
-            tma_load_4d(smem + S::kQ + x * kTileBytes + s * 16384, &tmap_q, &bar_q_full, s * 64, h,
-                        pp * 256 + x * 128, b);
-      }
-      __syncwarp();
-      ++q_it;
-      for (int j = 0; j < n; ++j, ++kv_it) {
-        const int kt = list[j];
-        const int st = kv_it % kStages;
-        const uint32_t ph = ((kv_it / kStages) & 1) ^ 1;
-        if (!wait1(&bar_k_empty[st], ph, kSiteKEmpty)) { alive = false; break; }
+  // Register reallocation inside each role (a softmax thread holds a whole
+  // 128-key row of S in registers).
+  if (warp >= 8) {
+    // warpgroup 2 hands registers to the softmax groups; warps 10-11 idle
+    regs_dec<kRegsOther>();
+    if (warp == kTmaWarp) {
+      // ------------------------------------------------------------ producer
+      uint32_t kv_it = 0, q_it = 0;
+      bool alive = true;
+      auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+        bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
+        return __shfl_sync(0xffffffffu, ok, 0);
+      };
+      for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+        const int tile = p.q_order[w / p.H];
+        const int h = static_cast<int>(w % p.H);
+        const int b = tile / nP, pp = tile % nP;
+        const int n = p.row_count[tile];
+        if (n == 0) continue;
+        const int32_t* list = p.row_list + static_cast<size_t>(tile) * nK;
+        if (!wait1(&bar_q_empty, (q_it & 1) ^ 1, kSiteQEmpty)) { alive = false; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_k_full[st], kTileBytes);
-#pragma unroll
-          for (int s = 0; s < D / 64; ++s)
-            tma_load_4d(smem + S::kK + st * kTileBytes + s * 16384, &tmap_k, &bar_k_full[st], s * 64, h, kt * 128, b);
+          mbar_arrive_expect_tx(&bar_q_full, 2 * kTileBytes);
+  #pragma unroll
+          for (int x = 0; x < 2; ++x)
+  #pragma unroll
+            for (int s = 0; s < D / 64; ++s)
+              tma_load_4d(smem + S::kQ + x * kTileBytes + s * 16384, &tmap_q, &bar_q_full, s * 64, h,
+                          pp * 256 + x * 128, b);
         }
         __syncwarp();
-        if (!wait1(&bar_v_empty[st], ph, kSiteVEmpty)) { alive = false; break; }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_v_full[st], kTileBytes);
-#pragma unroll
-          for (int s = 0; s < D / 64; ++s)
-            tma_load_4d(smem + S::kV + st * kTileBytes + s * 16384, &tmap_v, &bar_v_full[st], s * 64, h, kt * 128, b);
-        }
-        __syncwarp();
-      }
-    }
-    if (abort_s && lane == 0) {
-      // let copies still in flight land before the CTA leaves
-      if (q_it > 0) mbar_drain(&bar_q_full, (q_it - 1) & 1, 100000000ull);
-      for (uint32_t it = kv_it > kStages ? kv_it - kStages : 0; it <= kv_it; ++it) {
-        mbar_drain(&bar_k_full[it % kStages], (it / kStages) & 1, 100000000ull);
-        mbar_drain(&bar_v_full[it % kStages], (it / kStages) & 1, 100000000ull);
-      }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
-    constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
-    uint32_t kv_it = 0, q_it = 0, p_it = 0, o_it = 0;
-    bool alive = true;
-    auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
-      bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
-      return __shfl_sync(0xffffffffu, ok, 0);
-    };
-    auto issue_s = [&](int x, uint32_t idx) {  // S_x = Q_x K^T (K stage of key tile idx)
-      const int st = idx % kStages;
-      const uint32_t qbase = sQ + x * kTileBytes;
-      const uint32_t kbase = sK0 + st * kTileBytes;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        umma_ss(tmem + kColS + x * 128, kmajor_desc(qbase, kk), kmajor_desc(kbase, kk), idesc_s, kk > 0 ? 1u : 0u);
-      umma_commit(&bar_s_full[x]);
-    };
-    auto issue_pv = [&](int x, uint32_t idx, bool accumulate) {  // O_x += P_x V (P_x in TMEM)
-      const int st = idx % kStages;
-      const uint32_t vbase = sV0 + st * kTileBytes;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_ts(tmem + kColO + x * D, tmem + kColS + x * 128 + kk * 8, mnmajor_desc(vbase, kk), idesc_o,
-                (accumulate || kk > 0) ? 1u : 0u);
-      umma_commit(&bar_pv_done[x]);
-    };
-    for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
-      const int tile = p.q_order[w / p.H];
-      const int n = p.row_count[tile];
-      if (n == 0) continue;
-      if (!wait1(&bar_q_full, q_it & 1, kSiteQFull)) { alive = false; break; }
-      ++q_it;
-      const uint32_t base = kv_it;
-      if (!wait1(&bar_k_full[base % kStages], (base / kStages) & 1, kSiteKFull)) { alive = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
-        issue_s(0, base);
-        issue_s(1, base);
-        umma_commit(&bar_k_empty[base % kStages]);
-      }
-      __syncwarp();
-      for (int j = 0; j < n; ++j) {
-        const uint32_t idx = base + j;
-        const bool more = j + 1 < n;
-        if (!wait1(&bar_v_full[idx % kStages], (idx / kStages) & 1, kSiteVFull)) { alive = false; break; }
-        if (!wait1(&bar_p_full[0], p_it & 1, kSitePFull)) { alive = false; break; }
-        if (j == 0) {
-          if (!wait1(&bar_o_free, (o_it & 1) ^ 1, kSiteOFree)) { alive = false; break; }
-          ++o_it;
-        }
-        if (more && !wait1(&bar_k_full[(idx + 1) % kStages], ((idx + 1) / kStages) & 1, kSiteKFull)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        if (lane == 0) {
-          issue_pv(0, idx, j > 0);
-          if (more) issue_s(0, idx + 1);
-        }
-        __syncwarp();
-        if (!wait1(&bar_p_full[1], p_it & 1, kSitePFull)) { alive = false; break; }
-        tc_fence_after();
-        if (lane == 0) {
-          issue_pv(1, idx, j > 0);
-          umma_commit(&bar_v_empty[idx % kStages]);
-          if (more) {
-            issue_s(1, idx + 1);
-            umma_commit(&bar_k_empty[(idx + 1) % kStages]);
+        ++q_it;
+        for (int j = 0; j < n; ++j, ++kv_it) {
+          const int kt = list[j];
+          const int st = kv_it % kStages;
+          const uint32_t ph = ((kv_it / kStages) & 1) ^ 1;
+          if (!wait1(&bar_k_empty[st], ph, kSiteKEmpty)) { alive = false; break; }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bar_k_full[st], kTileBytes);
+  #pragma unroll
+            for (int s = 0; s < D / 64; ++s)
+              tma_load_4d(smem + S::kK + st * kTileBytes + s * 16384, &tmap_k, &bar_k_full[st], s * 64, h, kt * 128, b);
           }
+          __syncwarp();
+          if (!wait1(&bar_v_empty[st], ph, kSiteVEmpty)) { alive = false; break; }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bar_v_full[st], kTileBytes);
+  #pragma unroll
+            for (int s = 0; s < D / 64; ++s)
+              tma_load_4d(smem + S::kV + st * kTileBytes + s * 16384, &tmap_v, &bar_v_full[st], s * 64, h, kt * 128, b);
+          }
+          __syncwarp();
+        }
+      }
+      if (abort_s && lane == 0) {
+        // let copies still in flight land before the CTA leaves
+        if (q_it > 0) mbar_drain(&bar_q_full, (q_it - 1) & 1, 100000000ull);
+        for (uint32_t it = kv_it > kStages ? kv_it - kStages : 0; it <= kv_it; ++it) {
+          mbar_drain(&bar_k_full[it % kStages], (it / kStages) & 1, 100000000ull);
+          mbar_drain(&bar_v_full[it % kStages], (it / kStages) & 1, 100000000ull);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
+      uint32_t kv_it = 0, q_it = 0, p_it = 0, o_it = 0;
+      bool alive = true;
+      auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+        bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
+        return __shfl_sync(0xffffffffu, ok, 0);
+      };
+      auto issue_s = [&](int x, uint32_t idx) {  // S_x = Q_x K^T (K stage of key tile idx)
+        const int st = idx % kStages;
+        const uint32_t qbase = sQ + x * kTileBytes;
+        const uint32_t kbase = sK0 + st * kTileBytes;
+  #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + kColS + x * 128, kmajor_desc(qbase, kk), kmajor_desc(kbase, kk), idesc_s, kk > 0 ? 1u : 0u);
+        umma_commit(&bar_s_full[x]);
+      };
+      auto issue_pv = [&](int x, uint32_t idx, bool accumulate) {  // O_x += P_x V (P_x in TMEM)
+        const int st = idx % kStages;
+        const uint32_t vbase = sV0 + st * kTileBytes;
+  #pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + kColO + x * D, tmem + kColS + x * 128 + kk * 8, mnmajor_desc(vbase, kk), idesc_o,
+                  (accumulate || kk > 0) ? 1u : 0u);
+        umma_commit(&bar_pv_done[x]);
+      };
+      for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+        const int tile = p.q_order[w / p.H];
+        const int n = p.row_count[tile];
+        if (n == 0) continue;
+        if (!wait1(&bar_q_full, q_it & 1, kSiteQFull)) { alive = false; break; }
+        ++q_it;
+        const uint32_t base = kv_it;
+        if (!wait1(&bar_k_full[base % kStages], (base / kStages) & 1, kSiteKFull)) { alive = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          issue_s(0, base);
+          issue_s(1, base);
+          umma_commit(&bar_k_empty[base % kStages]);
         }
         __syncwarp();
-        ++p_it;
+        for (int j = 0; j < n; ++j) {
+          const uint32_t idx = base + j;
+          const bool more = j + 1 < n;
+          if (!wait1(&bar_v_full[idx % kStages], (idx / kStages) & 1, kSiteVFull)) { alive = false; break; }
+          if (!wait1(&bar_p_full[0], p_it & 1, kSitePFull)) { alive = false; break; }
+          if (j == 0) {
+            if (!wait1(&bar_o_free, (o_it & 1) ^ 1, kSiteOFree)) { alive = false; break; }
+            ++o_it;
+          }
+          if (more && !wait1(&bar_k_full[(idx + 1) % kStages], ((idx + 1) / kStages) & 1, kSiteKFull)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            issue_pv(0, idx, j > 0);
+            if (more) issue_s(0, idx + 1);
+          }
+          __syncwarp();
+          if (!wait1(&bar_p_full[1], p_it & 1, kSitePFull)) { alive = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            issue_pv(1, idx, j > 0);
+            umma_commit(&bar_v_empty[idx % kStages]);
+            if (more) {
+              issue_s(1, idx + 1);
+              umma_commit(&bar_k_empty[(idx + 1) % kStages]);
+            }
+          }
+          __syncwarp();
+          ++p_it;
+        }
+        kv_it = base + n;
+        if (!alive) break;
+        if (lane == 0) umma_commit(&bar_q_empty);
+        __syncwarp();
       }
-      kv_it = base + n;
-      if (!alive) break;
-      if (lane == 0) umma_commit(&bar_q_empty);
+      // every MMA issued by this thread has finished before TMEM is released
+      if (lane == 0) {
+        umma_commit(&bar_final);
+        mbar_drain(&bar_final, 0, 100000000ull);
+      }
       __syncwarp();
     }
-    // every MMA issued by this thread has finished before TMEM is released
-    if (lane == 0) {
-      umma_commit(&bar_final);
-      mbar_drain(&bar_final, 0, 100000000ull);
-    }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax
+    regs_inc<kRegsSoftmax>();
     const int x = warp >> 2;            // query tile of the pair: 0 = A, 1 = B
     const int row = threadIdx.x & 127;  // query row inside the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -430,20 +448,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!waitw(&bar_s_full[x], s_it & 1, kSiteSFull)) { alive = false; break; }
         ++s_it;
         tc_fence_after();
-        // pass 1: row max (FULL tiles need no mask)
+        // S row into registers (PARTIAL tiles: inadmissible keys -> -inf)
+        uint32_t srow[4][32];
         float mx;
-        if (!partial) mx = row_max<false>(s_col, seq_row, p.L, kt, my_seq);
-        else mx = row_max<true>(s_col, seq_row, p.L, kt, my_seq);
+        if (!partial) mx = load_row<false>(s_col, srow, seq_row, p.L, kt, my_seq);
+        else mx = load_row<true>(s_col, srow, seq_row, p.L, kt, my_seq);
         const float mx2 = mx * p.scale_log2;
         const bool grow = mx2 > m_ref + kRescaleThreshold;
         const float m_new = grow ? mx2 : m_ref;
         const float alpha = grow ? ex2(m_ref - m_new) : 1.0f;
         const bool any = m_new != -INFINITY;
         const float neg_m = any ? -m_new : 0.0f;
-        // pass 2: P = 2^(scale*log2e*S - m), packed bf16 over S columns [0, 64)
-        float lsum;
-        if (!partial) lsum = exp_store<false>(s_col, seq_row, p.L, kt, my_seq, any, p.scale_log2, neg_m);
-        else lsum = exp_store<true>(s_col, seq_row, p.L, kt, my_seq, any, p.scale_log2, neg_m);
+        // P = 2^(scale*log2e*S - m), packed bf16 over S columns [0, 64)
+        const float lsum = exp_store(s_col, srow, p.scale_log2, neg_m);
         l = l * alpha + lsum;
         // PV_x of the previous key tile has completed (S_x of this tile was
         // issued after it); rescale O_x when the max grew.
