@@ -325,9 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
       uint32_t kv_it = 0, q_it = 0, p_it = 0, o_it = 0;
       bool alive = true;
+      // All lanes wait (no divergence to rejoin); one lane issues.
       auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
-        bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
-        return __shfl_sync(0xffffffffu, ok, 0);
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
       };
       auto issue_s = [&](int x, uint32_t idx) {  // S_x = Q_x K^T (K stage of key tile idx)
         const int st = idx % kStages;
@@ -365,16 +365,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < n; ++j) {
           const uint32_t idx = base + j;
           const bool more = j + 1 < n;
-          if (!wait1(&bar_v_full[idx % kStages], (idx / kStages) & 1, kSiteVFull)) { alive = false; break; }
-          if (!wait1(&bar_p_full[0], p_it & 1, kSitePFull)) { alive = false; break; }
-          if (j == 0) {
-            if (!wait1(&bar_o_free, (o_it & 1) ^ 1, kSiteOFree)) { alive = false; break; }
-            ++o_it;
+          // Everything PV_A(j) and S_A(j+1) need: V(j), P_A(j), O free (first
+          // key tile), K(j+1).  Usually all are there already: test them at
+          // once and fall back to the waits one by one.
+          const uint32_t pv = (idx / kStages) & 1, pk = ((idx + 1) / kStages) & 1;
+          const bool ready = mbar_try_wait(&bar_v_full[idx % kStages], pv) & mbar_try_wait(&bar_p_full[0], p_it & 1) &
+                             (j > 0 || mbar_try_wait(&bar_o_free, (o_it & 1) ^ 1)) &
+                             (!more || mbar_try_wait(&bar_k_full[(idx + 1) % kStages], pk));
+          if (!__all_sync(0xffffffffu, ready)) {
+            if (!wait1(&bar_v_full[idx % kStages], pv, kSiteVFull)) { alive = false; break; }
+            if (!wait1(&bar_p_full[0], p_it & 1, kSitePFull)) { alive = false; break; }
+            if (j == 0 && !wait1(&bar_o_free, (o_it & 1) ^ 1, kSiteOFree)) { alive = false; break; }
+            if (more && !wait1(&bar_k_full[(idx + 1) % kStages], pk, kSiteKFull)) { alive = false; break; }
           }
-          if (more && !wait1(&bar_k_full[(idx + 1) % kStages], ((idx + 1) / kStages) & 1, kSiteKFull)) {
-            alive = false;
-            break;
-          }
+          if (j == 0) ++o_it;
           tc_fence_after();
           if (lane == 0) {
             issue_pv(0, idx, j > 0);

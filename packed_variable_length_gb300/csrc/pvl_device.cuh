@@ -72,15 +72,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete yet is suspended
+// until it completes or `hint_ns` nanoseconds pass, instead of polling; a
+// waiting warp then takes no issue slots or shared-memory cycles from the
+// warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // ctl.timeout_ns (records a timeout at `where`) or when another thread of the
-// CTA has aborted; returns false in both cases.
+// CTA has aborted; returns false in both cases.  The abort flag and the clock
+// are looked at about once a millisecond at most (the suspension limit).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const KernelCtl& ctl,
                                           uint32_t where) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     if (*ctl.abort) return false;
     if (global_timer_ns() - t0 > ctl.timeout_ns) {
       raise_error(ctl, kDevErrTimeout, where);
