@@ -375,9 +375,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_dq = idesc_bf16(128, D, true, true);      // dQ
     uint32_t kv_it = 0, qi = 0, item_it = 0;
     bool alive = true;
+    // All lanes wait (no divergence to rejoin); one lane issues.  Where two
+    // barriers gate the next MMA, both are tested at once first.
     auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
-      bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
-      return __shfl_sync(0xffffffffu, ok, 0);
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
+    };
+    auto ready2 = [&](uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
+      return __all_sync(0xffffffffu, mbar_try_wait(b0, p0) & mbar_try_wait(b1, p1));
     };
     for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
       const int tile = p.k_order[w / p.H];
@@ -398,8 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // dP^T overwrites the columns dQ of the previous query tile used
-        if (!wait1(&bar_dq_free, (qi & 1) ^ 1, kSiteDqFree)) { alive = false; break; }
-        if (!wait1(&bar_do_full, qi & 1, kSiteDoFull)) { alive = false; break; }
+        if (!ready2(&bar_dq_free, (qi & 1) ^ 1, &bar_do_full, qi & 1)) {
+          if (!wait1(&bar_dq_free, (qi & 1) ^ 1, kSiteDqFree)) { alive = false; break; }
+          if (!wait1(&bar_do_full, qi & 1, kSiteDoFull)) { alive = false; break; }
+        }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
