@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_kv_empty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_q_full[s], 1);
-      mbar_init(&bar_q_empty[s], 1);
+      mbar_init(&bar_q_empty[s], 1 + kComputeThreads / 32);  // dK MMA done + each compute warp's dQ reads
     }
     mbar_init(&bar_do_full, 1);
     mbar_init(&bar_do_empty, 1);
@@ -461,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per-warp dQ staging: one 32-row x 32-float buffer (slice 0)
     uint8_t* stage = smem + S::kStage + warp * 4096;
     uint32_t qi = 0, md_it = 0;
+    int pend_q = -1;  // Q stage whose dQ staging reads are still to be released
     bool alive = true;
     auto waitw = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
@@ -494,10 +495,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // acquire this tile's LSE / Delta / seq_id rows (their phase can not
         // advance before the dV MMA, which waits for this group)
         if (!waitw(&bar_do_full, qi & 1, kSiteDoFullC)) { alive = false; break; }
-        // this warp's dS^T slice held two dQ chunks of the previous tile: their
-        // reductions must have finished reading it
-        if (lane == 0) bulk_wait_group_read<0>();
-        __syncwarp();
         tc_fence_after();
         if (!partial)
           pds_chunks<false>(tmem + lane_base, g, row, sDST, lse2_s, delta_s, qseq_s, my_seq, p.scale_log2);
@@ -507,6 +504,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(&bar_ps_full);
+        // the previous tile's dQ reductions read this warp's staging buffer
+        // and its part of that tile's Q stage: once they have, the stage goes
+        // back to the producer (its next load is two tiles ahead)
+        if (pend_q >= 0) {
+          if (lane == 0) {
+            bulk_wait_group_read<0>();
+            mbar_arrive(&bar_q_empty[pend_q]);
+          }
+          __syncwarp();
+          pend_q = -1;
+        }
         if (!waitw(&bar_dq_ready, qi & 1, kSiteDqReady)) { alive = false; break; }
         tc_fence_after();
         uint32_t r[kHalfChunks][32];
@@ -518,10 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dQ_i rows of this warp (32 query rows x this group's D/2 columns) ->
         // fp32 accumulator with TMA reductions of 32 x 32 slices.  Slice 0 goes
         // through the warp's staging buffer, slice 1 (D = 128) through the
-        // warp's own 4 KB of the dS^T tile once the dQ / dK MMAs are done with
-        // it; padding rows add exact zeros, boxes wholly past L are skipped.
+        // warp's 4 KB of this tile's Q stage once the dK MMA has read Q_i (the
+        // stage is handed back to the producer after the reductions read it);
+        // padding rows add exact zeros, boxes wholly past L are skipped.
         const int row0 = qt * 128 + (warp & 3) * 32;
-        uint8_t* dst_slice = smem + S::kDST + g * 16384 + (warp & 3) * 4096;
+        const int qst = static_cast<int>(qi % kStages);
+        uint8_t* dst_slice = smem + S::kQ + qst * S::kTile + warp * 4096;
 #pragma unroll
         for (int c = 0; c < kHalfChunks; ++c) {
           if (c == 1) {
@@ -547,6 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++md_it;
         }
         if (lane == 0) bulk_commit_group();
+        pend_q = qst;
       }
       if (!alive) break;
       // epilogue: the last tile's mma_done (waited above) covers every dV / dK
@@ -579,7 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bar_acc_free);
     }
     // every dQ reduction of this warp has completed before the CTA leaves
-    if (lane == 0) bulk_wait_group_all();
+    if (lane == 0) {
+      bulk_wait_group_all();
+      if (pend_q >= 0) mbar_arrive(&bar_q_empty[pend_q]);
+    }
     __syncwarp();
   }
 
