@@ -17,11 +17,13 @@
 //   warp 8      TMA producer: the Q pair once per item, K and V tiles into
 //               separate 2-stage rings (a K stage frees as soon as both S
 //               MMAs that read it are done).
-//   warp 9      owns TMEM (512 columns: S_A, S_B, O_A, O_B) and issues
-//               tcgen05.mma from one thread in the order
-//               PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ...
-//               so the tensor core works on one query tile while the other
-//               tile's softmax runs.  PV reads P straight from TMEM.
+//   warps 9, 10 issue tcgen05.mma from one thread each, warp 9 for tile A
+//               (and owns TMEM: S_A, S_B, O_A, O_B, 512 columns), warp 10
+//               for tile B, each bracket PV_x(j), S_x(j+1); a turn token
+//               keeps the brackets in the order A, B, A, B, ..., so the
+//               tensor core works on one query tile while the other tile's
+//               softmax runs, and each issuer checks its gates while the
+//               other one issues.  PV reads P straight from TMEM.
 //   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: thread t owns
 //               query row t (TMEM lane t).  The whole 128-key row of S comes
 //               into registers with one TMEM wait (warpgroup 2 gives up
@@ -42,15 +44,16 @@
 namespace pvl {
 namespace {
 
-// warps 0-7 softmax (two warpgroups), 8 TMA, 9 MMA, 10-11 idle: they complete
-// the third warpgroup, whose registers go to the softmax groups
+// warps 0-7 softmax (two warpgroups), 8 TMA, 9 and 10 MMA issuers (tiles A
+// and B), 11 idle; warpgroup 2's registers go to the softmax groups
 constexpr int kThreads = 384;
 // registers per thread after reallocation: 256 x 208 + 128 x 88 = 384 x 168,
 // the launch's own allotment (168 = 65536 / 384 rounded down to 8)
 constexpr uint32_t kRegsSoftmax = 208;
 constexpr uint32_t kRegsOther = 88;
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // MMA issuer of query tile A; owns TMEM
+constexpr int kMmaWarpB = 10;  // MMA issuer of query tile B
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S_X at [128 X, 128 X + 128); P_X packed over its first 64 columns
@@ -59,7 +62,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum FwdSite : uint32_t {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull, kSitePFull, kSiteOFree,
-  kSiteSFull, kSitePvDone
+  kSiteSFull, kSitePvDone, kSiteTurn
 };
 
 template <int D>
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using S = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q_full, bar_q_empty, bar_o_free, bar_final;
+  __shared__ uint64_t bar_q_full, bar_q_empty, bar_o_free[2], bar_final[2], bar_turn[2];
   __shared__ uint64_t bar_k_full[kStages], bar_k_empty[kStages], bar_v_full[kStages], bar_v_empty[kStages];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2];
   __shared__ uint32_t tmem_base_s;
@@ -220,16 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_s = 0;
     mbar_init(&bar_q_full, 1);
-    mbar_init(&bar_q_empty, 1);
-    mbar_init(&bar_o_free, 256);
-    mbar_init(&bar_final, 1);
+    mbar_init(&bar_q_empty, 2);  // both MMA issuers
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_k_full[s], 1);
-      mbar_init(&bar_k_empty[s], 1);
+      mbar_init(&bar_k_empty[s], 2);
       mbar_init(&bar_v_full[s], 1);
-      mbar_init(&bar_v_empty[s], 1);
+      mbar_init(&bar_v_empty[s], 2);
     }
     for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_o_free[x], 128);
+      mbar_init(&bar_final[x], 1);
+      mbar_init(&bar_turn[x], 1);
       mbar_init(&bar_s_full[x], 1);
       mbar_init(&bar_p_full[x], 128);
       mbar_init(&bar_pv_done[x], 1);
@@ -259,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Register reallocation inside each role (a softmax thread holds a whole
   // 128-key row of S in registers).
   if (warp >= 8) {
-    // warpgroup 2 hands registers to the softmax groups; warps 10-11 idle
+    // warpgroup 2 hands registers to the softmax groups; warp 11 idles
     regs_dec<kRegsOther>();
     if (warp == kTmaWarp) {
       // ------------------------------------------------------------ producer
@@ -319,33 +323,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-    } else if (warp == kMmaWarp) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == kMmaWarp || warp == kMmaWarpB) {
+      // -------------------------------------------------------- MMA issuers
+      // Warp 9 issues the brackets of query tile A (S_A of the item's first
+      // key tile, then PV_A(j), S_A(j+1) for each j), warp 10 those of tile B.
+      // A turn token makes them strictly alternate A, B, A, B, ..., so the
+      // tensor core still runs one tile's MMAs while the other tile's softmax
+      // runs; each issuer tests its own gates while the other one issues,
+      // which takes the gate tests and barrier round trips off the tensor
+      // core's path.  K and V stages and the Q pair are released by both
+      // issuers (barrier counts of 2).
+      const int x = warp == kMmaWarp ? 0 : 1;
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
-      uint32_t kv_it = 0, q_it = 0, p_it = 0, o_it = 0;
+      uint32_t kv_it = 0, q_it = 0, p_it = 0, o_it = 0, turn_it = 0;
       bool alive = true;
       // All lanes wait (no divergence to rejoin); one lane issues.
       auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
       };
-      auto issue_s = [&](int x, uint32_t idx) {  // S_x = Q_x K^T (K stage of key tile idx)
-        const int st = idx % kStages;
-        const uint32_t qbase = sQ + x * kTileBytes;
-        const uint32_t kbase = sK0 + st * kTileBytes;
-  #pragma unroll
+      // this issuer's turn: tile A's k-th bracket follows tile B's (k-1)-th,
+      // tile B's k-th follows tile A's k-th
+      auto wait_turn = [&]() {
+        const uint32_t parity = x == 0 ? (turn_it & 1) ^ 1 : (turn_it & 1);
+        return wait1(&bar_turn[x], parity, kSiteTurn);
+      };
+      auto pass_turn = [&]() {
+        ++turn_it;
+        if (lane == 0) mbar_arrive(&bar_turn[x ^ 1]);
+        __syncwarp();
+      };
+      const uint32_t qbase = sQ + x * kTileBytes;
+      auto issue_s = [&](uint32_t idx) {  // S_x = Q_x K^T (K stage of key tile idx)
+        const uint32_t kbase = sK0 + (idx % kStages) * kTileBytes;
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + kColS + x * 128, kmajor_desc(qbase, kk), kmajor_desc(kbase, kk), idesc_s, kk > 0 ? 1u : 0u);
         umma_commit(&bar_s_full[x]);
+        umma_commit(&bar_k_empty[idx % kStages]);
       };
-      auto issue_pv = [&](int x, uint32_t idx, bool accumulate) {  // O_x += P_x V (P_x in TMEM)
-        const int st = idx % kStages;
-        const uint32_t vbase = sV0 + st * kTileBytes;
-  #pragma unroll
+      auto issue_pv = [&](uint32_t idx, bool accumulate) {  // O_x += P_x V (P_x in TMEM)
+        const uint32_t vbase = sV0 + (idx % kStages) * kTileBytes;
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ts(tmem + kColO + x * D, tmem + kColS + x * 128 + kk * 8, mnmajor_desc(vbase, kk), idesc_o,
                   (accumulate || kk > 0) ? 1u : 0u);
         umma_commit(&bar_pv_done[x]);
+        umma_commit(&bar_v_empty[idx % kStages]);
       };
       for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
         const int tile = p.q_order[w / p.H];
@@ -355,58 +379,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++q_it;
         const uint32_t base = kv_it;
         if (!wait1(&bar_k_full[base % kStages], (base / kStages) & 1, kSiteKFull)) { alive = false; break; }
+        if (!wait_turn()) { alive = false; break; }
         tc_fence_after();
-        if (lane == 0) {
-          issue_s(0, base);
-          issue_s(1, base);
-          umma_commit(&bar_k_empty[base % kStages]);
-        }
+        if (lane == 0) issue_s(base);
         __syncwarp();
+        pass_turn();
         for (int j = 0; j < n; ++j) {
           const uint32_t idx = base + j;
           const bool more = j + 1 < n;
-          // Everything PV_A(j) and S_A(j+1) need: V(j), P_A(j), O free (first
-          // key tile), K(j+1).  Usually all are there already: test them at
-          // once and fall back to the waits one by one.
+          // Everything PV_x(j) and S_x(j+1) need: V(j), P_x(j), O_x free
+          // (first key tile), K(j+1).  Usually all are there already: test
+          // them at once and fall back to the waits one by one.
           const uint32_t pv = (idx / kStages) & 1, pk = ((idx + 1) / kStages) & 1;
-          const bool ready = mbar_try_wait(&bar_v_full[idx % kStages], pv) & mbar_try_wait(&bar_p_full[0], p_it & 1) &
-                             (j > 0 || mbar_try_wait(&bar_o_free, (o_it & 1) ^ 1)) &
+          const bool ready = mbar_try_wait(&bar_v_full[idx % kStages], pv) & mbar_try_wait(&bar_p_full[x], p_it & 1) &
+                             (j > 0 || mbar_try_wait(&bar_o_free[x], (o_it & 1) ^ 1)) &
                              (!more || mbar_try_wait(&bar_k_full[(idx + 1) % kStages], pk));
           if (!__all_sync(0xffffffffu, ready)) {
             if (!wait1(&bar_v_full[idx % kStages], pv, kSiteVFull)) { alive = false; break; }
-            if (!wait1(&bar_p_full[0], p_it & 1, kSitePFull)) { alive = false; break; }
-            if (j == 0 && !wait1(&bar_o_free, (o_it & 1) ^ 1, kSiteOFree)) { alive = false; break; }
+            if (!wait1(&bar_p_full[x], p_it & 1, kSitePFull)) { alive = false; break; }
+            if (j == 0 && !wait1(&bar_o_free[x], (o_it & 1) ^ 1, kSiteOFree)) { alive = false; break; }
             if (more && !wait1(&bar_k_full[(idx + 1) % kStages], pk, kSiteKFull)) { alive = false; break; }
           }
           if (j == 0) ++o_it;
-          tc_fence_after();
-          if (lane == 0) {
-            issue_pv(0, idx, j > 0);
-            if (more) issue_s(0, idx + 1);
-          }
-          __syncwarp();
-          if (!wait1(&bar_p_full[1], p_it & 1, kSitePFull)) { alive = false; break; }
-          tc_fence_after();
-          if (lane == 0) {
-            issue_pv(1, idx, j > 0);
-            umma_commit(&bar_v_empty[idx % kStages]);
-            if (more) {
-              issue_s(1, idx + 1);
-              umma_commit(&bar_k_empty[(idx + 1) % kStages]);
-            }
-          }
-          __syncwarp();
           ++p_it;
+          if (!wait_turn()) { alive = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            issue_pv(idx, j > 0);
+            if (more) issue_s(idx + 1);
+          }
+          __syncwarp();
+          pass_turn();
         }
         kv_it = base + n;
         if (!alive) break;
         if (lane == 0) umma_commit(&bar_q_empty);
         __syncwarp();
       }
+      if (!alive && lane == 0) mbar_arrive(&bar_turn[x ^ 1]);  // let the other issuer notice the abort
       // every MMA issued by this thread has finished before TMEM is released
       if (lane == 0) {
-        umma_commit(&bar_final);
-        mbar_drain(&bar_final, 0, 100000000ull);
+        umma_commit(&bar_final[x]);
+        mbar_drain(&bar_final[x], 0, 100000000ull);
       }
       __syncwarp();
     }
@@ -514,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&bar_o_free);
+      mbar_arrive(&bar_o_free[x]);
       if (in_range) *lse_out = l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
