@@ -281,6 +281,14 @@ def run_gpu(args):
     h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("q", "k", "v", "do"))
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
 
+    # tile efficiency: unmasked pairs / pairs inside the tiles the kernels
+    # compute (FULL + PARTIAL), forward on 256 x 128 tiles, backward on 128 x 128
+    tmh = pvl.tile_map_build(sid, ws=tm_ws)
+    tile_eff = {}
+    for name, level, area in (("fwd", 1, 256 * 128), ("bwd", 0, 128 * 128)):
+        cls = tmh.to_host(level)["cls"]
+        tile_eff[name] = round(pairs / (int((cls > 0).sum()) * area), 4)
+
     peaks = load_peaks()
     peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
     value = world * flops / (ms_step * 1e-3) / 1e12
@@ -303,6 +311,7 @@ def run_gpu(args):
             "workload": describe(lay, valid_tokens),
             "B": B, "L": L, "H": H, "D": D, "tokens_per_frame": T,
             "unmasked_pairs_per_head": pairs,
+            "tile_efficiency": tile_eff,
             "step": "pack_build_seq_ids + tile_map_build + masked_attn_fwd + masked_attn_bwd",
             "l2": f"inputs larger than L2 (Q, K, V, dO are {dev['q'].numel() * 2 / 1e6:.0f} MB each); no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",

@@ -25,6 +25,14 @@ A query with s_i = -1 has no admissible key: O_i = 0, LSE_i = -inf, dQ_i = 0.
 A key with s_j = -1 is never admissible: dK_j = dV_j = 0.  The pages fix no
 softmax scale; the default is 1 / sqrt(D).
 
+Cross attention ("lingbot_va_packing" §2.1: the latent and the action tokens
+carry their own seq_ids, and frames past an episode's valid length drop out
+of the self and of the cross attention mask): queries q [B, Lq] with ids s_i
+and keys k, v [B, Lk] with their own ids t_j, M_ij = [s_i == t_j and
+s_i >= 0]; everything else is as above.  A valid query whose id has no key
+gets O_i = 0, LSE_i = -inf, dQ_i = 0, like a padding row.  Self attention is
+the case t = s (k_seq_id omitted).
+
 The sums over {j : M_ij} are evaluated by enumerating that set: for each id
 s >= 0 the positions holding s form the query rows and the key columns of one
 dense softmax.  Query rows are taken ``block`` at a time (summation order only).
@@ -55,28 +63,41 @@ def _groups(seq_row: np.ndarray):
         yield int(s), np.nonzero(seq_row == s)[0]
 
 
-def _check(q, seq_id):
-    if len(q.shape) != 4:
+def _check(q, k, seq_id, k_seq_id):
+    if len(q.shape) != 4 or len(k.shape) != 4:
         raise ValueError("expected [B, L, H, D]")
-    B, L, _, _ = q.shape
-    if tuple(np.asarray(seq_id).shape) != (B, L):
-        raise ValueError("seq_id must be [B, L]")
+    B, Lq, H, D = q.shape
+    if k.shape[0] != B or k.shape[2] != H or k.shape[3] != D:
+        raise ValueError("q and k differ in B, H or D")
+    if tuple(np.asarray(seq_id).shape) != (B, Lq):
+        raise ValueError("seq_id must be [B, Lq]")
+    if tuple(np.asarray(k_seq_id).shape) != (B, k.shape[1]):
+        raise ValueError("k_seq_id must be [B, Lk]")
 
 
-def attention_fwd(q, k, v, seq_id, scale: float | None = None, heads=None, block: int = 512):
-    """Returns (O [B, L, nh, D], LSE [B, nh, L]) in fp64 for the listed heads."""
-    _check(q, seq_id)
+def _pairs(q_row: np.ndarray, k_row: np.ndarray):
+    """(query positions, key positions) for every id >= 0 of the query row."""
+    for s, rows in _groups(q_row):
+        yield rows, np.nonzero(np.asarray(k_row) == s)[0]
+
+
+def attention_fwd(q, k, v, seq_id, scale: float | None = None, heads=None, block: int = 512, k_seq_id=None):
+    """Returns (O [B, Lq, nh, D], LSE [B, nh, Lq]) in fp64 for the listed heads."""
+    k_seq_id = seq_id if k_seq_id is None else k_seq_id
+    _check(q, k, seq_id, k_seq_id)
     B, L, H, D = q.shape
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     heads = list(range(H)) if heads is None else list(heads)
-    seq_id = np.asarray(seq_id)
+    seq_id, k_seq_id = np.asarray(seq_id), np.asarray(k_seq_id)
     O = np.zeros((B, L, len(heads), D))
     LSE = np.full((B, len(heads), L), -np.inf)
     for b in range(B):
         for hi, h in enumerate(heads):
             qb, kb, vb = _f64(q[b, :, h]), _f64(k[b, :, h]), _f64(v[b, :, h])
-            for _, idx in _groups(seq_id[b]):
-                Ks, Vs = kb[idx], vb[idx]
+            for idx, kidx in _pairs(seq_id[b], k_seq_id[b]):
+                if len(kidx) == 0:
+                    continue  # no admissible key: O = 0, LSE = -inf
+                Ks, Vs = kb[kidx], vb[kidx]
                 for i0 in range(0, len(idx), block):
                     rows = idx[i0:i0 + block]
                     S = scale * (qb[rows] @ Ks.T)
@@ -88,25 +109,30 @@ def attention_fwd(q, k, v, seq_id, scale: float | None = None, heads=None, block
     return O, LSE
 
 
-def attention_bwd(q, k, v, do, seq_id, scale: float | None = None, heads=None, block: int = 512):
-    """Returns (dQ, dK, dV [B, L, nh, D], Delta [B, nh, L]) in fp64 for the listed heads.
+def attention_bwd(q, k, v, do, seq_id, scale: float | None = None, heads=None, block: int = 512, k_seq_id=None):
+    """Returns (dQ [B, Lq, nh, D], dK, dV [B, Lk, nh, D], Delta [B, nh, Lq]) in
+    fp64 for the listed heads.
 
     Recomputes P from its own LSE; nothing produced by a kernel enters here.
     """
-    _check(q, seq_id)
+    k_seq_id = seq_id if k_seq_id is None else k_seq_id
+    _check(q, k, seq_id, k_seq_id)
     B, L, H, D = q.shape
+    Lk = k.shape[1]
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     heads = list(range(H)) if heads is None else list(heads)
-    seq_id = np.asarray(seq_id)
+    seq_id, k_seq_id = np.asarray(seq_id), np.asarray(k_seq_id)
     dQ = np.zeros((B, L, len(heads), D))
-    dK = np.zeros((B, L, len(heads), D))
-    dV = np.zeros((B, L, len(heads), D))
+    dK = np.zeros((B, Lk, len(heads), D))
+    dV = np.zeros((B, Lk, len(heads), D))
     Delta = np.zeros((B, len(heads), L))
     for b in range(B):
         for hi, h in enumerate(heads):
             qb, kb, vb, dob = _f64(q[b, :, h]), _f64(k[b, :, h]), _f64(v[b, :, h]), _f64(do[b, :, h])
-            for _, idx in _groups(seq_id[b]):
-                Ks, Vs = kb[idx], vb[idx]
+            for idx, kidx in _pairs(seq_id[b], k_seq_id[b]):
+                if len(kidx) == 0:
+                    continue  # no admissible key: dQ = 0, Delta = 0
+                Ks, Vs = kb[kidx], vb[kidx]
                 dKs = np.zeros_like(Ks)
                 dVs = np.zeros_like(Vs)
                 for i0 in range(0, len(idx), block):
@@ -122,16 +148,18 @@ def attention_bwd(q, k, v, do, seq_id, scale: float | None = None, heads=None, b
                     dKs += scale * (dS.T @ qb[rows])
                     dVs += P.T @ dob[rows]
                     Delta[b, hi, rows] = delta
-                dK[b, idx, hi] = dKs
-                dV[b, idx, hi] = dVs
+                dK[b, kidx, hi] = dKs
+                dV[b, kidx, hi] = dVs
     return dQ, dK, dV, Delta
 
 
-def effective_pairs(seq_id) -> int:
-    """Number of admissible (query, key) pairs per head: sum over rows and ids of n_id^2."""
+def effective_pairs(seq_id, k_seq_id=None) -> int:
+    """Admissible (query, key) pairs per head: sum over rows and ids of
+    (queries with the id) * (keys with the id); n_id^2 for self attention."""
     seq_id = np.asarray(seq_id)
+    k_seq_id = seq_id if k_seq_id is None else np.asarray(k_seq_id)
     total = 0
     for b in range(seq_id.shape[0]):
-        for _, idx in _groups(seq_id[b]):
-            total += len(idx) ** 2
+        for idx, kidx in _pairs(seq_id[b], k_seq_id[b]):
+            total += len(idx) * len(kidx)
     return total

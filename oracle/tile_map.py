@@ -7,7 +7,9 @@ size and no classification rule; the rule below is the plain reading of "skip
 a block when no pair in it can match, drop the per-element mask when every
 pair matches", made checkable from per-tile summaries only:
 
-- a position p of row b is *valid* iff p < L and seq_id[b, p] >= 0;
+- a position p of row b is *valid* iff p < L and seq_id[b, p] >= 0 (query
+  tiles over the query ids and length, key tiles over the key ids and length;
+  for cross attention, "lingbot_va_packing" §2.1, the two differ);
 - per tile t (block_m rows for query tiles, block_n for key tiles):
   nv = number of valid positions, lo / hi = min / max id over them;
 - (q-tile, k-tile) is EMPTY if nv_q == 0 or nv_k == 0 or hi_q < lo_k or
@@ -74,11 +76,16 @@ def _longest_first(counts_flat: np.ndarray) -> np.ndarray:
     return np.array([i for _, i in sorted(keys)], dtype=np.int32)
 
 
-def build_tile_map(seq_id: np.ndarray, L: int, block_m: int = 128, block_n: int = 128) -> dict:
+def build_tile_map(seq_id: np.ndarray, L: int, block_m: int = 128, block_n: int = 128,
+                   k_seq_id: np.ndarray | None = None, Lk: int | None = None) -> dict:
+    """Tile map of queries (seq_id, length L) against keys (k_seq_id, length
+    Lk; the queries' own when omitted)."""
     seq_id = np.asarray(seq_id)
+    k_seq_id = seq_id if k_seq_id is None else np.asarray(k_seq_id)
+    Lk = L if Lk is None else int(Lk)
     B = seq_id.shape[0]
     nTq = -(-L // block_m)
-    nTk = -(-L // block_n)
+    nTk = -(-Lk // block_n)
     cls = np.zeros((B, nTq, nTk), np.uint8)
     q_nv = np.zeros((B, nTq), np.int32)
     q_lo = np.zeros((B, nTq), np.int32)
@@ -94,7 +101,7 @@ def build_tile_map(seq_id: np.ndarray, L: int, block_m: int = 128, block_n: int 
     col_full = np.zeros((B, nTk), np.int32)
     for b in range(B):
         q_nv[b], q_lo[b], q_hi[b] = tile_stats(seq_id[b], L, block_m)
-        k_nv[b], k_lo[b], k_hi[b] = tile_stats(seq_id[b], L, block_n)
+        k_nv[b], k_lo[b], k_hi[b] = tile_stats(k_seq_id[b], Lk, block_n)
         for qt in range(nTq):
             for kt in range(nTk):
                 cls[b, qt, kt] = _classify(q_nv[b, qt], q_lo[b, qt], q_hi[b, qt], block_m,
@@ -102,7 +109,7 @@ def build_tile_map(seq_id: np.ndarray, L: int, block_m: int = 128, block_n: int 
         row_list[b], row_count[b], row_full[b] = _lists(cls[b])
         col_list[b], col_count[b], col_full[b] = _lists(cls[b].T)
     return {
-        "B": B, "L": L, "block_m": block_m, "block_n": block_n, "nTq": nTq, "nTk": nTk,
+        "B": B, "L": L, "Lk": Lk, "block_m": block_m, "block_n": block_n, "nTq": nTq, "nTk": nTk,
         "q_nv": q_nv, "q_lo": q_lo, "q_hi": q_hi, "k_nv": k_nv, "k_lo": k_lo, "k_hi": k_hi,
         "cls": cls,
         "row_list": row_list, "row_count": row_count, "row_full": row_full,

@@ -26,6 +26,9 @@ MUTATIONS = {
     "padding_admitted": ("seq_row[seq_row >= 0]", "seq_row[seq_row >= -1]"),
     "ids_merged": ("np.nonzero(seq_row == s)[0]", "np.nonzero(seq_row >= s)[0]"),
     "missing_max_shift": ("P = np.exp(S - lse[:, None])\n                    O[", "P = np.exp(S - m[:, None])\n                    O["),
+    "keys_take_query_ids": ("yield rows, np.nonzero(np.asarray(k_row) == s)[0]", "yield rows, np.nonzero(np.asarray(q_row) == s)[0]"),
+    "dk_at_query_positions": ("dK[b, kidx, hi] = dKs", "dK[b, idx, hi] = dKs"),
+    "padding_keys_admitted": ("yield rows, np.nonzero(np.asarray(k_row) == s)[0]", "yield rows, np.nonzero((np.asarray(k_row) == s) | (np.asarray(k_row) < 0))[0]"),
 }
 
 

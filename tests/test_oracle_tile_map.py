@@ -105,3 +105,67 @@ def test_workload_class_counts(n):
                 q_eps = {e for e in eq if starts[e] < min((qt + 1) * 128, lay.L) and starts[e + 1] > qt * 128}
                 k_eps = {e for e in eq if starts[e] < min((kt + 1) * 128, lay.L) and starts[e + 1] > kt * 128}
                 assert check_sound_blocks[qt, kt] == bool(q_eps & k_eps)
+
+
+# ---------------------------------------------------------- cross attention
+def admissible_cross(qsid_row, ksid_row, Lq, Lk, bm, bn, qt, kt):
+    m = np.zeros((bm, bn), bool)
+    for a in range(bm):
+        for c in range(bn):
+            i, j = qt * bm + a, kt * bn + c
+            if i < Lq and j < Lk and qsid_row[i] >= 0 and qsid_row[i] == ksid_row[j]:
+                m[a, c] = True
+    return m
+
+
+def check_sound_cross(qsid, ksid, Lq, Lk, bm, bn, exact):
+    tm = oracle.build_tile_map(qsid, Lq, bm, bn, k_seq_id=ksid, Lk=Lk)
+    assert tm["cls"].shape == (qsid.shape[0], -(-Lq // bm), -(-Lk // bn))
+    for b in range(qsid.shape[0]):
+        for qt in range(tm["nTq"]):
+            for kt in range(tm["nTk"]):
+                m = admissible_cross(qsid[b], ksid[b], Lq, Lk, bm, bn, qt, kt)
+                c = tm["cls"][b, qt, kt]
+                if c == EMPTY:
+                    assert not m.any()
+                if c == FULL:
+                    assert m.all()
+                if m.all():
+                    assert c == FULL
+                if exact:
+                    assert (c == EMPTY) == (not m.any())
+    return tm
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_cross_monotone_layouts_exact(seed):
+    """Queries and keys of the same episodes laid out in the same order with
+    different tokens per frame (the latent / action streams)."""
+    rng = np.random.default_rng(200 + seed)
+    lay = wl.random_layout(rng, B=2, K=3, T=int(rng.integers(2, 6)), L=int(rng.integers(40, 90)), H=1, D=8)
+    Tk = int(rng.integers(1, 4))
+    Lk = int(lay.seg_frames.sum(axis=1).max()) * Tk + int(rng.integers(0, 9))
+    qsid = oracle.build_seq_ids(lay.seg_frames, lay.seg_valid, lay.tokens_per_frame, lay.L)
+    ksid = oracle.build_seq_ids(lay.seg_frames, lay.seg_valid, Tk, Lk)
+    bm, bn = [(8, 8), (8, 4), (16, 8), (4, 8)][seed]
+    tm = check_sound_cross(qsid, ksid, lay.L, Lk, bm, bn, exact=True)
+    check_lists(tm)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_cross_interleaved_ids_sound(seed):
+    rng = np.random.default_rng(300 + seed)
+    Lq, Lk = int(rng.integers(10, 60)), int(rng.integers(5, 40))
+    qsid = rng.integers(-1, 4, size=(2, Lq)).astype(np.int32)
+    ksid = rng.integers(-1, 5, size=(2, Lk)).astype(np.int32)
+    tm = check_sound_cross(qsid, ksid, Lq, Lk, 8, 8, exact=False)
+    check_lists(tm)
+
+
+def test_cross_with_own_ids_is_self():
+    rng = np.random.default_rng(7)
+    sid = rng.integers(-1, 3, size=(2, 50)).astype(np.int32)
+    a = oracle.build_tile_map(sid, 50, 8, 16)
+    b = oracle.build_tile_map(sid, 50, 8, 16, k_seq_id=sid, Lk=50)
+    for key in ("cls", "row_list", "col_list", "q_order", "k_order"):
+        np.testing.assert_array_equal(a[key], b[key])
