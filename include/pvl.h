@@ -96,7 +96,7 @@ PVL_API pvl_status pack_build_seq_ids(const int32_t* seg_frames, const int32_t* 
  *
  * Workspace (dev, caller-allocated, tile_map_ws_bytes() bytes, 256-byte
  * aligned) holds, at the byte offsets tile_map_layout() returns:
- *   HEADER      int32[16]  magic, version, B, L, block_m, block_n, nTq, nTk
+ *   HEADER      int32[16]  magic, version, B, Lq, block_m, block_n, nTq, nTk, Lk
  *   Q_NV/LO/HI  int32[B*nTq]      K_NV/LO/HI int32[B*nTk]
  *   CLS         uint8[B*nTq*nTk]  class of (b, qt, kt)
  *   ROW_COUNT   int32[B*nTq]  non-empty key tiles per query tile
@@ -108,7 +108,8 @@ PVL_API pvl_status pack_build_seq_ids(const int32_t* seg_frames, const int32_t* 
  *   Q_ORDER     int32[B*nTq]  b*nTq+qt sorted by descending ROW_COUNT, ties
  *                              by ascending index (longest work first)
  *   K_ORDER     int32[B*nTk]  the same over key tiles by COL_COUNT
- * nTq = ceil(L / block_m), nTk = ceil(L / block_n).
+ * nTq = ceil(Lq / block_m), nTk = ceil(Lk / block_n); Lq = Lk = L for the
+ * self-attention map of tile_map_build.
  *
  * The workspace holds PVL_TM_LEVELS such maps built from the same seq_ids:
  * level 0 at (block_m, block_n) and level 1 at (2*block_m, block_n), whose
@@ -143,6 +144,19 @@ PVL_API pvl_status tile_map_layout(int B, int L, int block_m, int block_n, size_
 PVL_API pvl_status tile_map_build(const int32_t* seq_id, int B, int L, int block_m, int block_n, void* tile_ws,
                           size_t ws_bytes, pvl_stream_t stream);
 
+/* Cross-attention tile map ("lingbot_va_packing" §2.1: the latent and the
+ * action tokens carry their own seq_ids, both dropping invalid frames from
+ * the self and cross attention masks): query tiles over q_seq_id (dev int32
+ * [B * Lq]), key tiles over k_seq_id (dev int32 [B * Lk]); the pair rule,
+ * lists, orders and errors are those of tile_map_build, with "valid" read on
+ * each side over its own ids and length.  tile_map_build(seq_id, B, L, ...)
+ * is tile_map_build_cross(seq_id, seq_id, B, L, L, ...). */
+PVL_API size_t tile_map_ws_bytes_cross(int B, int Lq, int Lk, int block_m, int block_n);
+PVL_API pvl_status tile_map_layout_cross(int B, int Lq, int Lk, int block_m, int block_n, size_t* offsets);
+PVL_API pvl_status tile_map_build_cross(const int32_t* q_seq_id, const int32_t* k_seq_id, int B, int Lq, int Lk,
+                                        int block_m, int block_n, void* tile_ws, size_t ws_bytes,
+                                        pvl_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * masked_attn_fwd — O = softmax(scale * Q K^T restricted to admissible keys) V.
  * Defines: "furniture_packing_variable_length" (attention masking by seq_id)
@@ -162,6 +176,18 @@ PVL_API pvl_status tile_map_build(const int32_t* seq_id, int B, int L, int block
 PVL_API pvl_status masked_attn_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, const int32_t* seq_id,
                            const void* tile_ws, int B, int L, int H, int D, float scale, pvl_bf16* o,
                            float* lse, pvl_stream_t stream);
+
+/* Cross attention: q dev bf16 [B, Lq, H, D] with ids q_seq_id [B, Lq]; k, v
+ * dev bf16 [B, Lk, H, D] with ids k_seq_id [B, Lk]; query i attends key j iff
+ * q_seq_id[i] == k_seq_id[j] >= 0.  tile_ws: tile_map_build_cross of these
+ * ids at 128 x 128.  o: dev bf16 [B, Lq, H, D]; lse: dev fp32 [B, H, Lq].  A
+ * query with no admissible key (seq_id -1, or an id no key carries) gets
+ * O = 0 and LSE = -inf.  Errors as masked_attn_fwd, lengths checked each on
+ * its side.  masked_attn_fwd is the case k_seq_id = seq_id, Lk = Lq = L. */
+PVL_API pvl_status masked_attn_fwd_cross(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v,
+                                         const int32_t* q_seq_id, const int32_t* k_seq_id, const void* tile_ws,
+                                         int B, int Lq, int Lk, int H, int D, float scale, pvl_bf16* o, float* lse,
+                                         pvl_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * masked_attn_bwd — gradients of the masked attention from the saved LSE.
@@ -186,6 +212,20 @@ PVL_API pvl_status masked_attn_bwd(const pvl_bf16* q, const pvl_bf16* k, const p
                            const pvl_bf16* dO, const float* lse, const int32_t* seq_id, const void* tile_ws,
                            int B, int L, int H, int D, float scale, pvl_bf16* dq, pvl_bf16* dk, pvl_bf16* dv,
                            void* ws, size_t ws_bytes, pvl_stream_t stream);
+
+/* Cross attention backward: q, o, dO, dq [B, Lq, H, D] and lse [B, H, Lq]
+ * on the query side, k, v, dk, dv [B, Lk, H, D] on the key side, ids and
+ * tile map as for masked_attn_fwd_cross.  Keys with seq_id -1 or an id no
+ * query carries get dK = dV = 0; queries without an admissible key get
+ * dQ = 0.  ws: masked_attn_bwd_ws_bytes_cross(B, Lq, Lk, H, D) bytes (the
+ * query-side arrays of masked_attn_bwd's workspace, over Lq). */
+PVL_API size_t masked_attn_bwd_ws_bytes_cross(int B, int Lq, int Lk, int H, int D);
+
+PVL_API pvl_status masked_attn_bwd_cross(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, const pvl_bf16* o,
+                                         const pvl_bf16* dO, const float* lse, const int32_t* q_seq_id,
+                                         const int32_t* k_seq_id, const void* tile_ws, int B, int Lq, int Lk, int H,
+                                         int D, float scale, pvl_bf16* dq, pvl_bf16* dk, pvl_bf16* dv, void* ws,
+                                         size_t ws_bytes, pvl_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * masked_attn_bwd_no_alloc — masked_attn_bwd for callers that cannot

@@ -28,6 +28,14 @@ SIGNATURES = {
                                  _p, _p, _p, _p, _c_size, _p]),
     "masked_attn_bwd_no_alloc": (_c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int,
                                           _c_float, _p, _p, _p, _p]),
+    "tile_map_ws_bytes_cross": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "tile_map_layout_cross": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _p]),
+    "tile_map_build_cross": (_c_int, [_p, _p, _c_int, _c_int, _c_int, _c_int, _c_int, _p, _c_size, _p]),
+    "masked_attn_fwd_cross": (_c_int, [_p, _p, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                       _p, _p, _p]),
+    "masked_attn_bwd_ws_bytes_cross": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "masked_attn_bwd_cross": (_c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                       _c_float, _p, _p, _p, _p, _c_size, _p]),
     "pvl_device_error": (_c_int, [_p]),
     "pvl_device_error_detail": (_c_int, [_p, _p]),
     "pvl_last_error_message": (ctypes.c_char_p, []),

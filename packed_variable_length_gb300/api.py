@@ -82,20 +82,26 @@ class TileMap:
     """Device workspace written by tile_map_build plus typed views of its arrays.
 
     Level 0 is the map at (block_m, block_n); level 1 the map at
-    (2 * block_m, block_n) over pairs of query tiles."""
+    (2 * block_m, block_n) over pairs of query tiles.  L is the query length,
+    Lk the key length (equal for self attention)."""
     ws: torch.Tensor
     B: int
     L: int
     block_m: int
     block_n: int
     offsets: tuple  # LEVELS * len(TM_FIELDS) byte offsets
+    Lk: int = 0     # 0: same as L
+
+    def __post_init__(self):
+        if not self.Lk:
+            self.Lk = self.L
 
     def blocks(self, level: int = 0):
         return (self.block_m * (2 if level else 1), self.block_n)
 
     def n_tiles(self, level: int = 0):
         bm, bn = self.blocks(level)
-        return -(-self.L // bm), -(-self.L // bn)
+        return -(-self.L // bm), -(-self.Lk // bn)
 
     @property
     def nTq(self) -> int:
@@ -124,32 +130,48 @@ class TileMap:
         out = {name: self.field(name, level).cpu().numpy() for name in TM_FIELDS}
         bm, bn = self.blocks(level)
         nq, nk = self.n_tiles(level)
-        out.update(B=self.B, L=self.L, block_m=bm, block_n=bn, nTq=nq, nTk=nk)
+        out.update(B=self.B, L=self.L, Lk=self.Lk, block_m=bm, block_n=bn, nTq=nq, nTk=nk)
         return out
 
 
-def tile_map_ws_bytes(B: int, L: int, block_m: int = 128, block_n: int = 128) -> int:
-    return int(_lib.load().tile_map_ws_bytes(B, L, block_m, block_n))
+def tile_map_ws_bytes(B: int, L: int, block_m: int = 128, block_n: int = 128, Lk: int | None = None) -> int:
+    if Lk is None:
+        return int(_lib.load().tile_map_ws_bytes(B, L, block_m, block_n))
+    return int(_lib.load().tile_map_ws_bytes_cross(B, L, Lk, block_m, block_n))
 
 
 def tile_map_build(seq_id: torch.Tensor, block_m: int = 128, block_n: int = 128,
-                   ws: torch.Tensor | None = None, stream=None) -> TileMap:
+                   ws: torch.Tensor | None = None, stream=None, k_seq_id: torch.Tensor | None = None) -> TileMap:
+    """Tile map of the seq_id mask; with k_seq_id (int32 [B, Lk]) the
+    cross-attention map of queries with ids seq_id against keys with ids
+    k_seq_id."""
     lib = _lib.load()
     if seq_id.dim() != 2:
         raise ValueError("seq_id must be [B, L]")
     _need_cuda(seq_id, "seq_id", torch.int32)
     B, L = seq_id.shape
-    nbytes = int(lib.tile_map_ws_bytes(B, L, block_m, block_n))
+    Lk = L
+    if k_seq_id is not None:
+        if k_seq_id.dim() != 2 or k_seq_id.shape[0] != B:
+            raise ValueError("k_seq_id must be [B, Lk]")
+        _need_cuda(k_seq_id, "k_seq_id", torch.int32)
+        Lk = k_seq_id.shape[1]
+    nbytes = int(lib.tile_map_ws_bytes_cross(B, L, Lk, block_m, block_n))
     if nbytes == 0:
         raise PvlError(PVL_ERR_INVALID_ARG, "bad tile map sizes")
     if ws is None:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=seq_id.device)
     offs = (ctypes.c_size_t * (TM_LEVELS * len(TM_FIELDS)))()
-    _check(lib.tile_map_layout(B, L, block_m, block_n, ctypes.addressof(offs)))
     with torch.cuda.device(seq_id.device):
-        _check(lib.tile_map_build(seq_id.data_ptr(), B, L, block_m, block_n, ws.data_ptr(), ws.numel(),
-                                  _stream(stream)))
-    return TileMap(ws, B, L, block_m, block_n, tuple(offs))
+        if k_seq_id is None:
+            _check(lib.tile_map_layout(B, L, block_m, block_n, ctypes.addressof(offs)))
+            _check(lib.tile_map_build(seq_id.data_ptr(), B, L, block_m, block_n, ws.data_ptr(), ws.numel(),
+                                      _stream(stream)))
+        else:
+            _check(lib.tile_map_layout_cross(B, L, Lk, block_m, block_n, ctypes.addressof(offs)))
+            _check(lib.tile_map_build_cross(seq_id.data_ptr(), k_seq_id.data_ptr(), B, L, Lk, block_m, block_n,
+                                            ws.data_ptr(), ws.numel(), _stream(stream)))
+    return TileMap(ws, B, L, block_m, block_n, tuple(offs), Lk)
 
 
 # ---------------------------------------------------------------- attention
@@ -159,15 +181,29 @@ def _qkv_shape(q: torch.Tensor):
     return tuple(q.shape)
 
 
-def masked_attn_fwd(q, k, v, seq_id, tile_map: TileMap, scale: float | None = None, o=None, lse=None,
-                    stream=None):
-    """(O bf16 [B, L, H, D], LSE fp32 [B, H, L]) of seq_id-masked softmax attention."""
+def _key_side(q, k, seq_id, k_seq_id, tile_map):
+    """Checks the key-side shapes; returns (Lk, key ids)."""
     B, L, H, D = _qkv_shape(q)
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _need_cuda(t, name, torch.bfloat16, (B, L, H, D))
+    Lk = L if k_seq_id is None else int(k.shape[1]) if k.dim() == 4 else -1
     _need_cuda(seq_id, "seq_id", torch.int32, (B, L))
-    if (tile_map.B, tile_map.L) != (B, L):
-        raise ValueError("tile map was built for another [B, L]")
+    if k_seq_id is not None:
+        _need_cuda(k_seq_id, "k_seq_id", torch.int32, (B, Lk))
+    if (tile_map.B, tile_map.L, tile_map.Lk) != (B, L, Lk):
+        raise ValueError("tile map was built for another [B, Lq, Lk]")
+    return Lk, (seq_id if k_seq_id is None else k_seq_id)
+
+
+def masked_attn_fwd(q, k, v, seq_id, tile_map: TileMap, scale: float | None = None, o=None, lse=None,
+                    stream=None, k_seq_id=None):
+    """(O bf16 [B, L, H, D], LSE fp32 [B, H, L]) of seq_id-masked softmax attention.
+
+    With k_seq_id (int32 [B, Lk]) it is cross attention: k and v are
+    [B, Lk, H, D] and query i attends key j iff seq_id[i] == k_seq_id[j] >= 0."""
+    B, L, H, D = _qkv_shape(q)
+    Lk, kid = _key_side(q, k, seq_id, k_seq_id, tile_map)
+    _need_cuda(q, "q", torch.bfloat16, (B, L, H, D))
+    for name, t in (("k", k), ("v", v)):
+        _need_cuda(t, name, torch.bfloat16, (B, Lk, H, D))
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if o is None:
         o = torch.empty_like(q)
@@ -175,42 +211,59 @@ def masked_attn_fwd(q, k, v, seq_id, tile_map: TileMap, scale: float | None = No
         lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
     _need_cuda(o, "o", torch.bfloat16, (B, L, H, D))
     _need_cuda(lse, "lse", torch.float32, (B, H, L))
+    lib = _lib.load()
     with torch.cuda.device(q.device):
-        _check(_lib.load().masked_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_id.data_ptr(),
-                                           tile_map.ws.data_ptr(), B, L, H, D, scale, o.data_ptr(),
-                                           lse.data_ptr(), _stream(stream)))
+        if k_seq_id is None:
+            _check(lib.masked_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_id.data_ptr(),
+                                       tile_map.ws.data_ptr(), B, L, H, D, scale, o.data_ptr(), lse.data_ptr(),
+                                       _stream(stream)))
+        else:
+            _check(lib.masked_attn_fwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_id.data_ptr(),
+                                             kid.data_ptr(), tile_map.ws.data_ptr(), B, L, Lk, H, D, scale,
+                                             o.data_ptr(), lse.data_ptr(), _stream(stream)))
     return o, lse
 
 
-def masked_attn_bwd_ws_bytes(B: int, L: int, H: int, D: int) -> int:
-    return int(_lib.load().masked_attn_bwd_ws_bytes(B, L, H, D))
+def masked_attn_bwd_ws_bytes(B: int, L: int, H: int, D: int, Lk: int | None = None) -> int:
+    if Lk is None:
+        return int(_lib.load().masked_attn_bwd_ws_bytes(B, L, H, D))
+    return int(_lib.load().masked_attn_bwd_ws_bytes_cross(B, L, Lk, H, D))
 
 
 def masked_attn_bwd(q, k, v, o, do, lse, seq_id, tile_map: TileMap, scale: float | None = None, dq=None,
-                    dk=None, dv=None, ws=None, stream=None):
-    """(dQ, dK, dV) bf16 [B, L, H, D] of the masked attention, from the saved LSE."""
+                    dk=None, dv=None, ws=None, stream=None, k_seq_id=None):
+    """(dQ, dK, dV) of the masked attention, from the saved LSE: dQ like q,
+    dK and dV like k (cross attention with k_seq_id, as masked_attn_fwd)."""
     B, L, H, D = _qkv_shape(q)
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+    Lk, kid = _key_side(q, k, seq_id, k_seq_id, tile_map)
+    for name, t in (("q", q), ("o", o), ("do", do)):
         _need_cuda(t, name, torch.bfloat16, (B, L, H, D))
+    for name, t in (("k", k), ("v", v)):
+        _need_cuda(t, name, torch.bfloat16, (B, Lk, H, D))
     _need_cuda(lse, "lse", torch.float32, (B, H, L))
-    _need_cuda(seq_id, "seq_id", torch.int32, (B, L))
-    if (tile_map.B, tile_map.L) != (B, L):
-        raise ValueError("tile map was built for another [B, L]")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _need_cuda(t, name, torch.bfloat16, (B, L, H, D))
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
+    _need_cuda(dq, "dq", torch.bfloat16, (B, L, H, D))
+    for name, t in (("dk", dk), ("dv", dv)):
+        _need_cuda(t, name, torch.bfloat16, (B, Lk, H, D))
     lib = _lib.load()
-    nbytes = int(lib.masked_attn_bwd_ws_bytes(B, L, H, D))
+    nbytes = int(lib.masked_attn_bwd_ws_bytes_cross(B, L, Lk, H, D))
     if ws is None:
         ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     with torch.cuda.device(q.device):
-        _check(lib.masked_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                                   lse.data_ptr(), seq_id.data_ptr(), tile_map.ws.data_ptr(), B, L, H, D, scale,
-                                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws.numel(),
-                                   _stream(stream)))
+        if k_seq_id is None:
+            _check(lib.masked_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                       lse.data_ptr(), seq_id.data_ptr(), tile_map.ws.data_ptr(), B, L, H, D,
+                                       scale, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                                       ws.numel(), _stream(stream)))
+        else:
+            _check(lib.masked_attn_bwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                             lse.data_ptr(), seq_id.data_ptr(), kid.data_ptr(),
+                                             tile_map.ws.data_ptr(), B, L, Lk, H, D, scale, dq.data_ptr(),
+                                             dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws.numel(),
+                                             _stream(stream)))
     return dq, dk, dv
 
 

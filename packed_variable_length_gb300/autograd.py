@@ -14,22 +14,25 @@ from . import api
 
 class _PackedAttention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, seq_id, tile_map, scale):
-        o, lse = api.masked_attn_fwd(q, k, v, seq_id, tile_map, scale)
-        ctx.save_for_backward(q, k, v, o, lse, seq_id)
+    def forward(ctx, q, k, v, seq_id, k_seq_id, tile_map, scale):
+        o, lse = api.masked_attn_fwd(q, k, v, seq_id, tile_map, scale, k_seq_id=k_seq_id)
+        ctx.save_for_backward(q, k, v, o, lse, seq_id, k_seq_id)
         ctx.tile_map = tile_map
         ctx.scale = scale
         return o
 
     @staticmethod
     def backward(ctx, do):
-        q, k, v, o, lse, seq_id = ctx.saved_tensors
-        dq, dk, dv = api.masked_attn_bwd(q, k, v, o, do.contiguous(), lse, seq_id, ctx.tile_map, ctx.scale)
-        return dq, dk, dv, None, None, None
+        q, k, v, o, lse, seq_id, k_seq_id = ctx.saved_tensors
+        dq, dk, dv = api.masked_attn_bwd(q, k, v, o, do.contiguous(), lse, seq_id, ctx.tile_map, ctx.scale,
+                                         k_seq_id=k_seq_id)
+        return dq, dk, dv, None, None, None, None
 
 
-def packed_attention(q, k, v, seq_id, tile_map=None, scale=None):
-    """O = masked softmax attention of bf16 [B, L, H, D] q/k/v under int32 [B, L] seq_id."""
+def packed_attention(q, k, v, seq_id, tile_map=None, scale=None, k_seq_id=None):
+    """O = masked softmax attention of bf16 [B, L, H, D] q/k/v under int32 [B, L]
+    seq_id; with k_seq_id (int32 [B, Lk]) cross attention of q [B, L, H, D]
+    against k, v [B, Lk, H, D] ("lingbot_va_packing" §2.1)."""
     if tile_map is None:
-        tile_map = api.tile_map_build(seq_id)
-    return _PackedAttention.apply(q, k, v, seq_id, tile_map, scale)
+        tile_map = api.tile_map_build(seq_id, k_seq_id=k_seq_id)
+    return _PackedAttention.apply(q, k, v, seq_id, k_seq_id, tile_map, scale)

@@ -6,6 +6,9 @@
 //   Delta_i = <dO_i, O_i>,  dS = P * (dO V^T - Delta),
 //   dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K.
 // Keys with seq_id -1 get dK = dV = 0 and queries with seq_id -1 get dQ = 0.
+// Cross attention ("lingbot_va_packing" §2.1): queries [B, Lq] and keys
+// [B, Lk] carry their own ids; a key (query) whose id no query (key) carries
+// also gets zero gradients.
 //
 // Three launches on the caller's stream:
 //   bwd_pre      Delta and LSE * log2(e) per query (fp32, padded to whole
@@ -81,15 +84,18 @@ struct BwdParams {
   const int32_t* col_full;
   const int32_t* col_list;
   const int32_t* k_order;
-  const int32_t* seq_id;  // [B, L]     key seq_ids
+  const int32_t* k_seq;   // [B, Lk]    key seq_ids
   const float* delta;     // [B, H, Lp]
   const float* lse2;      // [B, H, Lp] LSE * log2(e)
-  const int32_t* qseq;    // [B, Lp]    query seq_ids, -1 past L
+  const int32_t* qseq;    // [B, Lp]    query seq_ids, -1 past Lq
   float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   DeviceError* err;
-  int B, L, Lp, H, nT;
+  int B, Lq, Lk, Lp, H;
+  int nT;   // key tiles per row (items)
+  int nTq;  // query tiles per row: the length of each key tile's query list
+  // Lp: Lq rounded up to whole 128-row tiles
   long long total_items;
   float scale_log2;
   float scale;
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   {
     const int32_t* hd = p.header;
-    const bool ok = hd[0] == kTileMapMagic && hd[1] == kTileMapVersion && hd[2] == p.B && hd[3] == p.L &&
+    const bool ok = hd[0] == kTileMapMagic && hd[1] == kTileMapVersion && hd[2] == p.B && hd[3] == p.Lq && hd[8] == p.Lk &&
                     hd[4] == 128 && hd[5] == 128;
     if (!ok) {
       if (threadIdx.x == 0 && atomicCAS(&p.err->code, 0u, kDevErrTileMap) == 0u) p.err->block = blockIdx.x;
@@ -323,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = tile / nT, kt = tile % nT;
       const int n = p.col_count[tile];
       if (n == 0) continue;
-      const int32_t* list = p.col_list + static_cast<size_t>(tile) * nT;
+      const int32_t* list = p.col_list + static_cast<size_t>(tile) * p.nTq;
       if (!wait1(&bar_kv_empty, (kv_it & 1) ^ 1, kSiteKvEmpty)) { alive = false; break; }
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar_kv_full, 2 * kTileBytes);
@@ -472,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = tile / nT, kt = tile % nT;
       const int n = p.col_count[tile];
       const int kpos = kt * 128 + row;
-      const bool k_in = kpos < p.L;
-      const size_t krow = ((static_cast<size_t>(b) * p.L + kpos) * p.H + h) * D + g * kHalfD;
+      const bool k_in = kpos < p.Lk;
+      const size_t krow = ((static_cast<size_t>(b) * p.Lk + kpos) * p.H + h) * D + g * kHalfD;
       if (n == 0) {  // no valid key in this tile: zero gradients
         if (k_in) {
 #pragma unroll
@@ -485,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int nfull = p.col_full[tile];
-      const int32_t* list = p.col_list + static_cast<size_t>(tile) * nT;
-      const int my_seq = k_in ? p.seq_id[static_cast<size_t>(b) * p.L + kpos] : -1;
+      const int32_t* list = p.col_list + static_cast<size_t>(tile) * p.nTq;
+      const int my_seq = k_in ? p.k_seq[static_cast<size_t>(b) * p.Lk + kpos] : -1;
       for (int i = 0; i < n; ++i, ++qi) {
         const int qt = list[i];
         const bool partial = i >= nfull;
@@ -549,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          r[c][4 * v + 3]);
           fence_async_smem();
           __syncwarp();
-          if (lane == 0 && row0 < p.L) tma_reduce_add_4d(&tmap_dq, buf, g * kHalfD + 32 * c, h, row0, b);
+          if (lane == 0 && row0 >= 0 && row0 < p.Lq) tma_reduce_add_4d(&tmap_dq, buf, g * kHalfD + 32 * c, h, row0, b);
         }
         if (!alive) break;
         if (kHalfChunks < 2) {  // D = 64: the dS^T slice was not used, but the MMAs must still be waited for
@@ -615,13 +621,14 @@ int grid_for(long long work, int threads) {
 
 template <int D>
 pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, const pvl_bf16* o,
-                      const pvl_bf16* dO, const float* lse, const int32_t* seq_id, const void* tile_ws, int B,
-                      int L, int H, float scale, pvl_bf16* dq, pvl_bf16* dk, pvl_bf16* dv, void* ws,
-                      cudaStream_t stream) {
+                      const pvl_bf16* dO, const float* lse, const int32_t* q_seq, const int32_t* k_seq,
+                      const void* tile_ws, int B, int L, int Lk, int H, float scale, pvl_bf16* dq, pvl_bf16* dk,
+                      pvl_bf16* dv, void* ws, cudaStream_t stream) {
+  // L: queries (Lq), Lk: keys
   CUtensorMap tq, tk, tv, tdo, tdq;
   pvl_status st = make_bhld_tensor_map(&tq, q, B, L, H, D);
-  if (st == PVL_OK) st = make_bhld_tensor_map(&tk, k, B, L, H, D);
-  if (st == PVL_OK) st = make_bhld_tensor_map(&tv, v, B, L, H, D);
+  if (st == PVL_OK) st = make_bhld_tensor_map(&tk, k, B, Lk, H, D);
+  if (st == PVL_OK) st = make_bhld_tensor_map(&tv, v, B, Lk, H, D);
   if (st == PVL_OK) st = make_bhld_tensor_map(&tdo, dO, B, L, H, D);
   if (st != PVL_OK) return st;
   DeviceError* err = device_error_record();
@@ -639,19 +646,19 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   const long long rows = static_cast<long long>(B) * L * H;
 
   bwd_pre_kernel<D><<<grid_for(rows * (D / 8), 256), 256, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), lse, seq_id, delta, lse2,
+      reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), lse, q_seq, delta, lse2,
       qseq, dq_acc, B, L, Lp, H);
   st = check_cuda(cudaGetLastError(), "masked_attn_bwd preprocess launch");
   if (st != PVL_OK) return st;
 
-  const TileMapView tm = tile_map_view(tile_ws, B, L, 128, 128, 0);
+  const TileMapView tm = tile_map_view(tile_ws, B, L, Lk, 128, 128, 0);
   BwdParams prm;
   prm.header = tm.header;
   prm.col_count = tm.col_count;
   prm.col_full = tm.col_full;
   prm.col_list = tm.col_list;
   prm.k_order = tm.k_order;
-  prm.seq_id = seq_id;
+  prm.k_seq = k_seq;
   prm.delta = delta;
   prm.lse2 = lse2;
   prm.qseq = qseq;
@@ -660,10 +667,12 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   prm.dv = reinterpret_cast<__nv_bfloat16*>(dv);
   prm.err = err;
   prm.B = B;
-  prm.L = L;
+  prm.Lq = L;
+  prm.Lk = Lk;
   prm.Lp = Lp;
   prm.H = H;
   prm.nT = tm.nTk;
+  prm.nTq = tm.nTq;
   prm.total_items = static_cast<long long>(B) * tm.nTk * H;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.scale = scale;
@@ -687,26 +696,41 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
 
 using namespace pvl;
 
+extern "C" size_t masked_attn_bwd_ws_bytes_cross(int B, int Lq, int Lk, int H, int D) {
+  if (B < 1 || Lq < 1 || Lk < 1 || H < 1 || D < 1) return 0;
+  return bwd_ws_total_bytes(B, Lq, H, D);  // every scratch array is on the query side
+}
+
 extern "C" size_t masked_attn_bwd_ws_bytes(int B, int L, int H, int D) {
-  if (B < 1 || L < 1 || H < 1 || D < 1) return 0;
-  return bwd_ws_total_bytes(B, L, H, D);
+  return masked_attn_bwd_ws_bytes_cross(B, L, L, H, D);
+}
+
+extern "C" pvl_status masked_attn_bwd_cross(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v,
+                                            const pvl_bf16* o, const pvl_bf16* dO, const float* lse,
+                                            const int32_t* q_seq_id, const int32_t* k_seq_id, const void* tile_ws,
+                                            int B, int Lq, int Lk, int H, int D, float scale, pvl_bf16* dq,
+                                            pvl_bf16* dk, pvl_bf16* dv, void* ws, size_t ws_bytes,
+                                            pvl_stream_t stream) {
+  const void* ptrs[] = {q, k, v, o, dO, lse, q_seq_id, k_seq_id, tile_ws, dq, dk, dv, ws};
+  if (ws && ws_bytes < masked_attn_bwd_ws_bytes_cross(B, Lq, Lk, H, D))
+    return fail(PVL_ERR_INVALID_ARG, "masked_attn_bwd: workspace %zu bytes < %zu needed", ws_bytes,
+                masked_attn_bwd_ws_bytes_cross(B, Lq, Lk, H, D));
+  pvl_status st = validate_attn_qk("masked_attn_bwd", ptrs, 13, B, Lq, Lk, H, D, scale);
+  if (st != PVL_OK) return st;
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0)
+    return fail(PVL_ERR_INVALID_ARG, "masked_attn_bwd: workspace must be 256-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D == 64)
+    return launch_bwd<64>(q, k, v, o, dO, lse, q_seq_id, k_seq_id, tile_ws, B, Lq, Lk, H, scale, dq, dk, dv, ws, s);
+  return launch_bwd<128>(q, k, v, o, dO, lse, q_seq_id, k_seq_id, tile_ws, B, Lq, Lk, H, scale, dq, dk, dv, ws, s);
 }
 
 extern "C" pvl_status masked_attn_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, const pvl_bf16* o,
                                       const pvl_bf16* dO, const float* lse, const int32_t* seq_id,
                                       const void* tile_ws, int B, int L, int H, int D, float scale, pvl_bf16* dq,
                                       pvl_bf16* dk, pvl_bf16* dv, void* ws, size_t ws_bytes, pvl_stream_t stream) {
-  const void* ptrs[] = {q, k, v, o, dO, lse, seq_id, tile_ws, dq, dk, dv, ws};
-  if (ws && ws_bytes < masked_attn_bwd_ws_bytes(B, L, H, D))
-    return fail(PVL_ERR_INVALID_ARG, "masked_attn_bwd: workspace %zu bytes < %zu needed", ws_bytes,
-                masked_attn_bwd_ws_bytes(B, L, H, D));
-  pvl_status st = validate_attn("masked_attn_bwd", ptrs, 12, B, L, H, D, scale);
-  if (st != PVL_OK) return st;
-  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0)
-    return fail(PVL_ERR_INVALID_ARG, "masked_attn_bwd: workspace must be 256-byte aligned");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 64) return launch_bwd<64>(q, k, v, o, dO, lse, seq_id, tile_ws, B, L, H, scale, dq, dk, dv, ws, s);
-  return launch_bwd<128>(q, k, v, o, dO, lse, seq_id, tile_ws, B, L, H, scale, dq, dk, dv, ws, s);
+  return masked_attn_bwd_cross(q, k, v, o, dO, lse, seq_id, seq_id, tile_ws, B, L, L, H, D, scale, dq, dk, dv, ws,
+                               ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------------
@@ -764,6 +788,7 @@ extern "C" pvl_status masked_attn_bwd_no_alloc(const pvl_bf16* q, const pvl_bf16
   st = no_alloc_scratch(&scratch);
   if (st != PVL_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 64) return launch_bwd<64>(q, k, v, o, dO, lse, seq_id, tile_ws, B, L, H, scale, dq, dk, dv, scratch, s);
-  return launch_bwd<128>(q, k, v, o, dO, lse, seq_id, tile_ws, B, L, H, scale, dq, dk, dv, scratch, s);
+  if (D == 64)
+    return launch_bwd<64>(q, k, v, o, dO, lse, seq_id, seq_id, tile_ws, B, L, L, H, scale, dq, dk, dv, scratch, s);
+  return launch_bwd<128>(q, k, v, o, dO, lse, seq_id, seq_id, tile_ws, B, L, L, H, scale, dq, dk, dv, scratch, s);
 }

@@ -5,7 +5,10 @@
 // row b, head h and query i with s_i >= 0,
 //   O_i = sum_{j: s_j = s_i} softmax_j(scale * <q_i, k_j>) v_j,
 //   LSE_i = log sum_{j: s_j = s_i} exp(scale * <q_i, k_j>);
-// rows with s_i = -1 get O_i = 0 and LSE_i = -inf.
+// rows with s_i = -1 get O_i = 0 and LSE_i = -inf.  For cross attention
+// ("lingbot_va_packing" §2.1) the keys carry their own ids t_j and length Lk
+// (j: t_j = s_i above); a query whose id no key carries also gets O_i = 0,
+// LSE_i = -inf.
 //
 // Design.  One persistent CTA per SM walks work items (b, query-tile pair,
 // head): two adjacent 128-row query tiles A and B that share one stream of
@@ -78,7 +81,8 @@ struct FwdSmem {
 };
 
 struct FwdParams {
-  const int32_t* seq_id;
+  const int32_t* q_seq;      // [B, Lq] query seq_ids
+  const int32_t* k_seq;      // [B, Lk] key seq_ids (q_seq for self attention)
   const int32_t* header;     // level-1 map (256-row query tiles)
   const int32_t* row_count;
   const int32_t* row_full;
@@ -87,7 +91,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   DeviceError* err;
-  int B, L, H, nP, nK;       // query-tile pairs and key tiles per row
+  int B, Lq, Lk, H, nP, nK;  // query-tile pairs and key tiles per row
   long long total_items;  // tiles * H, heads innermost
   float scale_log2;
   uint64_t timeout_ns;
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The tile map must describe this call; otherwise do nothing.
   {
     const int32_t* hd = p.header;
-    const bool ok = hd[0] == kTileMapMagic && hd[1] == kTileMapVersion && hd[2] == p.B && hd[3] == p.L &&
+    const bool ok = hd[0] == kTileMapMagic && hd[1] == kTileMapVersion && hd[2] == p.B && hd[3] == p.Lq && hd[8] == p.Lk &&
                     hd[4] == 256 && hd[5] == 128;
     if (!ok) {
       if (threadIdx.x == 0 && atomicCAS(&p.err->code, 0u, kDevErrTileMap) == 0u) p.err->block = blockIdx.x;
@@ -443,9 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = tile / nP, pp = tile % nP;
       const int n = p.row_count[tile];
       const int qpos = pp * 256 + x * 128 + row;
-      const bool in_range = qpos < p.L;
-      __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.L + qpos) * p.H + h) * D;
-      float* lse_out = p.lse + (static_cast<size_t>(b) * p.H + h) * p.L + qpos;
+      const bool in_range = qpos < p.Lq;
+      __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Lq + qpos) * p.H + h) * D;
+      float* lse_out = p.lse + (static_cast<size_t>(b) * p.H + h) * p.Lq + qpos;
       if (n == 0) {  // no valid query in this pair of tiles
         if (in_range) {
 #pragma unroll
@@ -456,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int nfull = p.row_full[tile];
       const int32_t* list = p.row_list + static_cast<size_t>(tile) * nK;
-      const int32_t* seq_row = p.seq_id + static_cast<size_t>(b) * p.L;
-      const int my_seq = in_range ? seq_row[qpos] : -1;
+      const int32_t* seq_row = p.k_seq + static_cast<size_t>(b) * p.Lk;  // key ids of this row
+      const int my_seq = in_range ? p.q_seq[static_cast<size_t>(b) * p.Lq + qpos] : -1;
       float m_ref = -INFINITY;  // running max of scale*log2(e)*s
       float l = 0.0f;           // running sum of 2^(...) relative to m_ref
       for (int j = 0; j < n; ++j) {
@@ -469,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S row into registers (PARTIAL tiles: inadmissible keys -> -inf)
         uint32_t srow[4][32];
         float mx;
-        if (!partial) mx = load_row<false>(s_col, srow, seq_row, p.L, kt, my_seq);
-        else mx = load_row<true>(s_col, srow, seq_row, p.L, kt, my_seq);
+        if (!partial) mx = load_row<false>(s_col, srow, seq_row, p.Lk, kt, my_seq);
+        else mx = load_row<true>(s_col, srow, seq_row, p.Lk, kt, my_seq);
         const float mx2 = mx * p.scale_log2;
         const bool grow = mx2 > m_ref + kRescaleThreshold;
         const float m_new = grow ? mx2 : m_ref;
@@ -542,20 +546,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-pvl_status launch_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, const int32_t* seq_id,
-                      const void* tile_ws, int B, int L, int H, float scale, pvl_bf16* o, float* lse,
-                      cudaStream_t stream) {
+pvl_status launch_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, const int32_t* q_seq,
+                      const int32_t* k_seq, const void* tile_ws, int B, int Lq, int Lk, int H, float scale,
+                      pvl_bf16* o, float* lse, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
-  pvl_status st = make_bhld_tensor_map(&tq, q, B, L, H, D);
-  if (st == PVL_OK) st = make_bhld_tensor_map(&tk, k, B, L, H, D);
-  if (st == PVL_OK) st = make_bhld_tensor_map(&tv, v, B, L, H, D);
+  pvl_status st = make_bhld_tensor_map(&tq, q, B, Lq, H, D);
+  if (st == PVL_OK) st = make_bhld_tensor_map(&tk, k, B, Lk, H, D);
+  if (st == PVL_OK) st = make_bhld_tensor_map(&tv, v, B, Lk, H, D);
   if (st != PVL_OK) return st;
   DeviceError* err = device_error_record();
   const int sms = sm_count();
   if (!err || sms <= 0) return fail(PVL_ERR_CUDA, "masked_attn_fwd: no usable CUDA device");
-  const TileMapView tm = tile_map_view(tile_ws, B, L, 128, 128, 1);  // pairs of query tiles
+  const TileMapView tm = tile_map_view(tile_ws, B, Lq, Lk, 128, 128, 1);  // pairs of query tiles
   FwdParams prm;
-  prm.seq_id = seq_id;
+  prm.q_seq = q_seq;
+  prm.k_seq = k_seq;
   prm.header = tm.header;
   prm.row_count = tm.row_count;
   prm.row_full = tm.row_full;
@@ -565,7 +570,8 @@ pvl_status launch_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   prm.lse = lse;
   prm.err = err;
   prm.B = B;
-  prm.L = L;
+  prm.Lq = Lq;
+  prm.Lk = Lk;
   prm.H = H;
   prm.nP = tm.nTq;
   prm.nK = tm.nTk;
@@ -586,13 +592,20 @@ pvl_status launch_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
 
 using namespace pvl;
 
+extern "C" pvl_status masked_attn_fwd_cross(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v,
+                                            const int32_t* q_seq_id, const int32_t* k_seq_id, const void* tile_ws,
+                                            int B, int Lq, int Lk, int H, int D, float scale, pvl_bf16* o,
+                                            float* lse, pvl_stream_t stream) {
+  const void* ptrs[] = {q, k, v, q_seq_id, k_seq_id, tile_ws, o, lse};
+  const pvl_status st = validate_attn_qk("masked_attn_fwd", ptrs, 8, B, Lq, Lk, H, D, scale);
+  if (st != PVL_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D == 64) return launch_fwd<64>(q, k, v, q_seq_id, k_seq_id, tile_ws, B, Lq, Lk, H, scale, o, lse, s);
+  return launch_fwd<128>(q, k, v, q_seq_id, k_seq_id, tile_ws, B, Lq, Lk, H, scale, o, lse, s);
+}
+
 extern "C" pvl_status masked_attn_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, const int32_t* seq_id,
                                       const void* tile_ws, int B, int L, int H, int D, float scale, pvl_bf16* o,
                                       float* lse, pvl_stream_t stream) {
-  const void* ptrs[] = {q, k, v, seq_id, tile_ws, o, lse};
-  const pvl_status st = validate_attn("masked_attn_fwd", ptrs, 7, B, L, H, D, scale);
-  if (st != PVL_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 64) return launch_fwd<64>(q, k, v, seq_id, tile_ws, B, L, H, scale, o, lse, s);
-  return launch_fwd<128>(q, k, v, seq_id, tile_ws, B, L, H, scale, o, lse, s);
+  return masked_attn_fwd_cross(q, k, v, seq_id, seq_id, tile_ws, B, L, L, H, D, scale, o, lse, stream);
 }

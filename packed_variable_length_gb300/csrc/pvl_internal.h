@@ -30,7 +30,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 // --------------------------------------------------------- tile map layout
 constexpr int32_t kTileMapMagic = 0x544C5650;  // "PVLT"
-constexpr int32_t kTileMapVersion = 1;
+constexpr int32_t kTileMapVersion = 2;  // header: magic, version, B, Lq, bm, bn, nTq, nTk, Lk
 constexpr uint8_t kEmpty = 0, kPartial = 1, kFull = 2;
 
 PVL_HD inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -41,11 +41,12 @@ struct TileMapLayout {
   int nTq, nTk;
 };
 
-// One level of the map (block sizes bm x bn), starting at byte `base`.
-PVL_HD inline TileMapLayout tile_map_level_layout(int B, int L, int bm, int bn, size_t base) {
+// One level of the map (block sizes bm x bn) of Lq queries against Lk keys,
+// starting at byte `base`.
+PVL_HD inline TileMapLayout tile_map_level_layout(int B, int Lq, int Lk, int bm, int bn, size_t base) {
   TileMapLayout t{};
-  t.nTq = (L + bm - 1) / bm;
-  t.nTk = (L + bn - 1) / bn;
+  t.nTq = (Lq + bm - 1) / bm;
+  t.nTk = (Lk + bn - 1) / bn;
   const size_t nq = static_cast<size_t>(B) * t.nTq;
   const size_t nk = static_cast<size_t>(B) * t.nTk;
   const size_t nqk = nq * t.nTk;
@@ -76,10 +77,10 @@ struct TileMapLayouts {
   size_t total;
 };
 
-PVL_HD inline TileMapLayouts tile_map_layouts(int B, int L, int bm, int bn) {
+PVL_HD inline TileMapLayouts tile_map_layouts(int B, int Lq, int Lk, int bm, int bn) {
   TileMapLayouts r{};
-  r.level[0] = tile_map_level_layout(B, L, bm, bn, 0);
-  r.level[1] = tile_map_level_layout(B, L, 2 * bm, bn, r.level[0].total);
+  r.level[0] = tile_map_level_layout(B, Lq, Lk, bm, bn, 0);
+  r.level[1] = tile_map_level_layout(B, Lq, Lk, 2 * bm, bn, r.level[0].total);
   r.total = r.level[1].total;
   return r;
 }
@@ -99,8 +100,8 @@ struct TileMapView {
   int nTq, nTk;
 };
 
-inline TileMapView tile_map_view(const void* ws, int B, int L, int bm, int bn, int level) {
-  const TileMapLayout t = tile_map_layouts(B, L, bm, bn).level[level];
+inline TileMapView tile_map_view(const void* ws, int B, int Lq, int Lk, int bm, int bn, int level) {
+  const TileMapLayout t = tile_map_layouts(B, Lq, Lk, bm, bn).level[level];
   const char* p = static_cast<const char*>(ws);
   TileMapView v;
   v.header = reinterpret_cast<const int32_t*>(p + t.off[PVL_TM_HEADER]);
@@ -128,6 +129,9 @@ int sm_count();                                    // current device, 0 on failu
 // Shared argument checks of the attention calls: null pointers and sizes
 // (INVALID_ARG), D, alignment and limits (UNSUPPORTED).
 pvl_status validate_attn(const char* who, const void* const* ptrs, int nptrs, int B, int L, int H, int D, float scale);
+// The same for Lq queries against Lk keys (the query-side checks use Lq).
+pvl_status validate_attn_qk(const char* who, const void* const* ptrs, int nptrs, int B, int Lq, int Lk, int H, int D,
+                            float scale);
 
 // Backward workspace, each part 256-byte aligned: the fp32 dQ accumulator
 // [B, L, H, D]; then, over query positions padded to whole 128-row tiles

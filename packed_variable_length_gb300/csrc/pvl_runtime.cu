@@ -89,6 +89,18 @@ pvl_status validate_attn(const char* who, const void* const* ptrs, int nptrs, in
   return PVL_OK;
 }
 
+pvl_status validate_attn_qk(const char* who, const void* const* ptrs, int nptrs, int B, int Lq, int Lk, int H, int D,
+                            float scale) {
+  if (Lk < 1) return fail(PVL_ERR_INVALID_ARG, "%s: Lk must be >= 1", who);
+  if (Lk > PVL_MAX_L) return fail(PVL_ERR_UNSUPPORTED, "%s: Lk = %d exceeds %d", who, Lk, PVL_MAX_L);
+  if (static_cast<long long>(B) * Lk * H * D >= (1ll << 40))
+    return fail(PVL_ERR_UNSUPPORTED, "%s: key tensor of %lld elements is too large", who,
+                static_cast<long long>(B) * Lk * H * D);
+  if (static_cast<long long>(B) * ((Lk + 127) / 128) * H >= (1ll << 31))
+    return fail(PVL_ERR_UNSUPPORTED, "%s: too many work items", who);
+  return validate_attn(who, ptrs, nptrs, B, Lq, H, D, scale);
+}
+
 namespace {
 pvl_status encode_bhld(void* map_out, const void* base, CUtensorMapDataType type, int esize, int B, int L, int H,
                        int D, const cuuint32_t box[4], CUtensorMapSwizzle swizzle);

@@ -50,13 +50,18 @@ TileMapPtrs tile_map_ptrs(void* ws, const TileMapLayout& t) {
 constexpr int kStatThreads = 128;
 
 // grid (nTq + nTk, B): blocks [0, nTq) summarise query tiles of block_m
-// positions, the rest key tiles of block_n positions.
-__global__ void __launch_bounds__(kStatThreads) tile_stats_kernel(const int32_t* __restrict__ seq_id, int B, int L,
-                                                                  int bm, int bn, int nTq, int nTk, TileMapPtrs m) {
+// positions over the query ids, the rest key tiles of block_n positions over
+// the key ids (the same array for self attention).
+__global__ void __launch_bounds__(kStatThreads) tile_stats_kernel(const int32_t* __restrict__ q_seq,
+                                                                  const int32_t* __restrict__ k_seq, int B, int Lq,
+                                                                  int Lk, int bm, int bn, int nTq, int nTk,
+                                                                  TileMapPtrs m) {
   const int b = blockIdx.y;
   const bool is_q = blockIdx.x < nTq;
   const int t = is_q ? blockIdx.x : blockIdx.x - nTq;
   const int bs = is_q ? bm : bn;
+  const int L = is_q ? Lq : Lk;
+  const int32_t* seq_id = is_q ? q_seq : k_seq;
   int cnt = 0, lo = INT32_MAX, hi = INT32_MIN;
   for (int i = threadIdx.x; i < bs; i += kStatThreads) {
     const long long p = static_cast<long long>(t) * bs + i;
@@ -97,12 +102,13 @@ __global__ void __launch_bounds__(kStatThreads) tile_stats_kernel(const int32_t*
       m.header[0] = kTileMapMagic;
       m.header[1] = kTileMapVersion;
       m.header[2] = B;
-      m.header[3] = L;
+      m.header[3] = Lq;
       m.header[4] = bm;
       m.header[5] = bn;
       m.header[6] = nTq;
       m.header[7] = nTk;
-      for (int i = 8; i < 16; ++i) m.header[i] = 0;
+      m.header[8] = Lk;
+      for (int i = 9; i < 16; ++i) m.header[i] = 0;
     }
   }
 }
@@ -215,45 +221,34 @@ int next_pow2(int n) {
 
 using namespace pvl;
 
-extern "C" size_t tile_map_ws_bytes(int B, int L, int block_m, int block_n) {
-  if (B < 1 || L < 1 || block_m < 1 || block_n < 1) return 0;
-  return tile_map_layouts(B, L, block_m, block_n).total;
-}
+namespace pvl {
+namespace {
 
-extern "C" pvl_status tile_map_layout(int B, int L, int block_m, int block_n, size_t* offsets) {
-  if (!offsets) return fail(PVL_ERR_INVALID_ARG, "tile_map_layout: null offsets");
-  if (B < 1 || L < 1 || block_m < 1 || block_n < 1)
-    return fail(PVL_ERR_INVALID_ARG, "tile_map_layout: sizes must be >= 1");
-  const TileMapLayouts t = tile_map_layouts(B, L, block_m, block_n);
-  for (int lv = 0; lv < PVL_TM_LEVELS; ++lv)
-    for (int i = 0; i < PVL_TM_NFIELDS; ++i) offsets[lv * PVL_TM_NFIELDS + i] = t.level[lv].off[i];
-  return PVL_OK;
-}
-
-extern "C" pvl_status tile_map_build(const int32_t* seq_id, int B, int L, int block_m, int block_n, void* tile_ws,
-                                     size_t ws_bytes, pvl_stream_t stream) {
-  if (!seq_id || !tile_ws) return fail(PVL_ERR_INVALID_ARG, "tile_map_build: null pointer");
-  if (B < 1 || L < 1) return fail(PVL_ERR_INVALID_ARG, "tile_map_build: B and L must be >= 1");
+pvl_status build_tile_map(const char* who, const int32_t* q_seq, const int32_t* k_seq, int B, int Lq, int Lk,
+                          int block_m, int block_n, void* tile_ws, size_t ws_bytes, cudaStream_t s) {
+  if (!q_seq || !k_seq || !tile_ws) return fail(PVL_ERR_INVALID_ARG, "%s: null pointer", who);
+  if (B < 1 || Lq < 1 || Lk < 1) return fail(PVL_ERR_INVALID_ARG, "%s: B and the lengths must be >= 1", who);
   if (block_m < 1 || block_m > 1024 || block_n < 1 || block_n > 1024)
-    return fail(PVL_ERR_UNSUPPORTED, "tile_map_build: block sizes must be in 1..1024");
-  if (L > PVL_MAX_L) return fail(PVL_ERR_UNSUPPORTED, "tile_map_build: L = %d exceeds %d", L, PVL_MAX_L);
+    return fail(PVL_ERR_UNSUPPORTED, "%s: block sizes must be in 1..1024", who);
+  if (Lq > PVL_MAX_L || Lk > PVL_MAX_L)
+    return fail(PVL_ERR_UNSUPPORTED, "%s: length %d exceeds %d", who, Lq > Lk ? Lq : Lk, PVL_MAX_L);
   if (reinterpret_cast<uintptr_t>(tile_ws) % 256 != 0)
-    return fail(PVL_ERR_INVALID_ARG, "tile_map_build: workspace must be 256-byte aligned");
-  const TileMapLayouts all = tile_map_layouts(B, L, block_m, block_n);
+    return fail(PVL_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  const TileMapLayouts all = tile_map_layouts(B, Lq, Lk, block_m, block_n);
   if (ws_bytes < all.total)
-    return fail(PVL_ERR_INVALID_ARG, "tile_map_build: workspace %zu bytes < %zu needed", ws_bytes, all.total);
+    return fail(PVL_ERR_INVALID_ARG, "%s: workspace %zu bytes < %zu needed", who, ws_bytes, all.total);
   const long long nq0 = static_cast<long long>(B) * all.level[0].nTq, nk0 = static_cast<long long>(B) * all.level[0].nTk;
   if (nq0 > PVL_MAX_ORDER_TILES || nk0 > PVL_MAX_ORDER_TILES)
-    return fail(PVL_ERR_UNSUPPORTED, "tile_map_build: B * tiles = %lld exceeds %d", nq0 > nk0 ? nq0 : nk0,
+    return fail(PVL_ERR_UNSUPPORTED, "%s: B * tiles = %lld exceeds %d", who, nq0 > nk0 ? nq0 : nk0,
                 PVL_MAX_ORDER_TILES);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   for (int lv = 0; lv < PVL_TM_LEVELS; ++lv) {
     const TileMapLayout& t = all.level[lv];
     const int bm = lv == 0 ? block_m : 2 * block_m;
     const long long nq = static_cast<long long>(B) * t.nTq, nk = static_cast<long long>(B) * t.nTk;
     const TileMapPtrs m = tile_map_ptrs(tile_ws, t);
 
-    tile_stats_kernel<<<dim3(t.nTq + t.nTk, B), kStatThreads, 0, s>>>(seq_id, B, L, bm, block_n, t.nTq, t.nTk, m);
+    tile_stats_kernel<<<dim3(t.nTq + t.nTk, B), kStatThreads, 0, s>>>(q_seq, k_seq, B, Lq, Lk, bm, block_n, t.nTq,
+                                                                     t.nTk, m);
     pvl_status st = check_cuda(cudaGetLastError(), "tile_stats launch");
     if (st != PVL_OK) return st;
 
@@ -275,4 +270,47 @@ extern "C" pvl_status tile_map_build(const int32_t* seq_id, int B, int L, int bl
     if (st != PVL_OK) return st;
   }
   return PVL_OK;
+}
+
+pvl_status layout_offsets(const char* who, int B, int Lq, int Lk, int block_m, int block_n, size_t* offsets) {
+  if (!offsets) return fail(PVL_ERR_INVALID_ARG, "%s: null offsets", who);
+  if (B < 1 || Lq < 1 || Lk < 1 || block_m < 1 || block_n < 1)
+    return fail(PVL_ERR_INVALID_ARG, "%s: sizes must be >= 1", who);
+  const TileMapLayouts t = tile_map_layouts(B, Lq, Lk, block_m, block_n);
+  for (int lv = 0; lv < PVL_TM_LEVELS; ++lv)
+    for (int i = 0; i < PVL_TM_NFIELDS; ++i) offsets[lv * PVL_TM_NFIELDS + i] = t.level[lv].off[i];
+  return PVL_OK;
+}
+
+}  // namespace
+}  // namespace pvl
+
+extern "C" size_t tile_map_ws_bytes(int B, int L, int block_m, int block_n) {
+  return tile_map_ws_bytes_cross(B, L, L, block_m, block_n);
+}
+
+extern "C" size_t tile_map_ws_bytes_cross(int B, int Lq, int Lk, int block_m, int block_n) {
+  if (B < 1 || Lq < 1 || Lk < 1 || block_m < 1 || block_n < 1) return 0;
+  return tile_map_layouts(B, Lq, Lk, block_m, block_n).total;
+}
+
+extern "C" pvl_status tile_map_layout(int B, int L, int block_m, int block_n, size_t* offsets) {
+  return layout_offsets("tile_map_layout", B, L, L, block_m, block_n, offsets);
+}
+
+extern "C" pvl_status tile_map_layout_cross(int B, int Lq, int Lk, int block_m, int block_n, size_t* offsets) {
+  return layout_offsets("tile_map_layout_cross", B, Lq, Lk, block_m, block_n, offsets);
+}
+
+extern "C" pvl_status tile_map_build(const int32_t* seq_id, int B, int L, int block_m, int block_n, void* tile_ws,
+                                     size_t ws_bytes, pvl_stream_t stream) {
+  return build_tile_map("tile_map_build", seq_id, seq_id, B, L, L, block_m, block_n, tile_ws, ws_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" pvl_status tile_map_build_cross(const int32_t* q_seq_id, const int32_t* k_seq_id, int B, int Lq, int Lk,
+                                           int block_m, int block_n, void* tile_ws, size_t ws_bytes,
+                                           pvl_stream_t stream) {
+  return build_tile_map("tile_map_build_cross", q_seq_id, k_seq_id, B, Lq, Lk, block_m, block_n, tile_ws, ws_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
 }

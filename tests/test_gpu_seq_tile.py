@@ -26,8 +26,8 @@ def compare_tile_maps(got: dict, ref: dict):
     for key in ("q_nv", "q_lo", "q_hi", "k_nv", "k_lo", "k_hi", "cls", "row_count", "row_full", "row_list",
                 "col_count", "col_full", "col_list", "q_order", "k_order"):
         np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
-    assert list(got["header"][:8]) == [0x544C5650, 1, ref["B"], ref["L"], ref["block_m"], ref["block_n"],
-                                       ref["nTq"], ref["nTk"]]
+    assert list(got["header"][:9]) == [0x544C5650, 2, ref["B"], ref["L"], ref["block_m"], ref["block_n"],
+                                       ref["nTq"], ref["nTk"], ref["Lk"]]
 
 
 def layouts():

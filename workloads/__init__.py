@@ -14,6 +14,8 @@ replaced by uniform draws of F.
 """
 
 from .configs import (  # noqa: F401
+    ACTION_TOKENS_PER_FRAME,
+    CrossLayout,
     F_MAX,
     F_MIN,
     PAD_MULTIPLE,
@@ -21,6 +23,9 @@ from .configs import (  # noqa: F401
     Layout,
     bucket_sweep_layouts,
     config_layout,
+    cross_config_layout,
+    cross_layout,
+    make_cross_tensors,
     make_tensors,
     random_layout,
     round_up,

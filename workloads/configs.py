@@ -24,6 +24,13 @@ Workloads (seed = 1000 + workload number):
    160 lengths F ~ U{103..362}, pool 200, each batch padded to
    round_up(max F, 8).
 
+Cross attention ("lingbot_va_packing" §2.1: the latent and the action tokens
+carry their own seq_ids): a ``CrossLayout`` pairs a query layout (the latent
+stream) with a key stream over the same segment table at its own tokens per
+frame and length.  The pages give no action-token count; 16 per latent frame
+is this build's choice.  Cross workloads: workloads 2, 3 and 4 as queries,
+keys at 16 tokens per frame, key length the longest row rounded up to 64.
+
 Values are standard normal (numpy PCG64, platform independent) rounded to bf16
 with round-to-nearest-even; the upstream gradient dO is drawn on every row,
 padding rows included, so a leak through padding would show.
@@ -39,6 +46,7 @@ import torch
 from .sampler import LengthBucketBatchSampler
 
 TOKENS_PER_FRAME = 38
+ACTION_TOKENS_PER_FRAME = 16
 PAD_MULTIPLE = 8
 F_MIN, F_MAX = 103, 362
 SEQ_CAP = 65536
@@ -154,5 +162,63 @@ def make_tensors(layout: Layout, device="cpu", with_grad_out: bool = True):
     out = {}
     for nm in names:
         x = rng.standard_normal(size=shape, dtype=np.float32)
+        out[nm] = torch.from_numpy(x).to(torch.bfloat16).to(device)
+    return out
+
+
+@dataclasses.dataclass
+class CrossLayout:
+    """Queries over ``q`` (its segments, tokens per frame and length); keys and
+    values over the same segments at ``tokens_per_frame_k`` tokens per frame
+    and length ``Lk``."""
+    q: Layout
+    tokens_per_frame_k: int
+    Lk: int
+
+    @property
+    def name(self) -> str:
+        return "cross_" + self.q.name
+
+    @property
+    def B(self) -> int:
+        return self.q.B
+
+    @property
+    def H(self) -> int:
+        return self.q.H
+
+    @property
+    def D(self) -> int:
+        return self.q.D
+
+    @property
+    def Lq(self) -> int:
+        return self.q.L
+
+
+def cross_layout(q: Layout, tokens_per_frame_k: int = ACTION_TOKENS_PER_FRAME, Lk: int | None = None) -> CrossLayout:
+    """Key length: the longest row rounded up to 64 by default; an explicit
+    Lk is raised to the longest row if it is shorter."""
+    need = int(q.seg_frames.sum(axis=1).max()) * int(tokens_per_frame_k)
+    if Lk is None:
+        Lk = int(round_up(need, 64))
+    return CrossLayout(q, int(tokens_per_frame_k), max(int(Lk), need, 1))
+
+
+def cross_config_layout(n: int) -> CrossLayout:
+    """Cross workload over workload ``n`` in 2..4."""
+    if n not in (2, 3, 4):
+        raise ValueError(f"no cross layout for workload {n}")
+    return cross_layout(config_layout(n))
+
+
+def make_cross_tensors(cl: CrossLayout, device="cpu", with_grad_out: bool = True):
+    """Q (and dO) as bf16 [B, Lq, H, D], K and V as bf16 [B, Lk, H, D], drawn
+    in the order q, k, v, dO from the query layout's seed + 7."""
+    rng = np.random.default_rng(cl.q.seed + 7)
+    out = {}
+    for nm in ["q", "k", "v"] + (["do"] if with_grad_out else []):
+        L = cl.Lk if nm in ("k", "v") else cl.Lq
+        x = rng.standard_normal(size=(cl.B, L, cl.H, cl.D), dtype=np.float32)
         out[nm] = torch.from_numpy(x).to(torch.bfloat16).to(device)
     return out
