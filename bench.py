@@ -12,6 +12,11 @@ backward 10 D flops per pair and head).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
+`--workload cross_concat64k` (or cross_padded) measures cross attention
+instead: the same episodes as queries at 38 tokens per frame and as keys at 16
+tokens per frame, each side with its own seq_ids (12 launches per step: one
+seq_id build per side).
+
 Under torchrun (N > 1) every rank runs an independent replica of the step on
 its own GPU (the path has no exchange step); rank 0 prints one JSON line.
 `--impl reference` times the fp64 CPU oracle on this host's cores instead
@@ -52,10 +57,13 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def unmasked_pairs(lay) -> int:
-    """Pairs per head: every segment's real tokens form one id (distinct ids per segment)."""
+def unmasked_pairs(lay, tokens_per_frame_k=None) -> int:
+    """Pairs per head: every segment's real tokens form one id (distinct ids per
+    segment); for cross attention queries at the layout's tokens per frame and
+    keys at tokens_per_frame_k."""
     T = lay.tokens_per_frame
-    return int(sum(int(v) * T * int(v) * T for row in lay.seg_valid for v in row))
+    Tk = T if tokens_per_frame_k is None else tokens_per_frame_k
+    return int(sum(int(v) * T * int(v) * Tk for row in lay.seg_valid for v in row))
 
 
 # ------------------------------------------------------------------ clocks
@@ -146,7 +154,7 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def traffic_record(kernel_file: str):
+def traffic_record(kernel_file: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -156,15 +164,20 @@ def traffic_record(kernel_file: str):
     src = os.path.join(ROOT, "packed_variable_length_gb300", "csrc", kernel_file)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     entry = rec.get(kernel_file)
-    if not entry or entry.get("source_sha") != sha:
+    if not entry or entry.get("source_sha") != sha or entry.get("workload") != workload:
         return None
     return entry.get("dram_bytes_per_launch")
 
 
-WORKLOADS = {"concat64k": 4, "padded": 3, "same_length": 2}
+# name -> (workload number, cross attention?)
+WORKLOADS = {"concat64k": (4, False), "padded": (3, False), "same_length": (2, False),
+             "cross_concat64k": (4, True), "cross_padded": (3, True)}
 
 
-def describe(lay, valid_tokens: int) -> str:
+def describe(lay, valid_tokens: int, cl=None) -> str:
+    if cl is not None:
+        return (describe(lay, valid_tokens) + f"; cross attention: queries as above, keys and values the same "
+                f"episodes at {cl.tokens_per_frame_k} tokens/frame (Lk = {cl.Lk}), each side with its own seq_ids")
     if lay.name == "concat64k":
         return (f"concat64k: one packed row of {lay.K} episodes (latent F = {lay.seg_frames[0].tolist()}, "
                 f"{lay.tokens_per_frame} tokens/frame, {valid_tokens} valid tokens) padded with seq_id -1 to "
@@ -174,17 +187,21 @@ def describe(lay, valid_tokens: int) -> str:
             f"H = {lay.H}, D = {lay.D}")
 
 
-def cpu_baseline(lay, tensors, budget_heads=1):
+def cpu_baseline(lay, tensors, budget_heads=1, cl=None):
     """The fp64 oracle as it stands on this host's cores: fwd + bwd of one head
     over every episode of the workload."""
     import oracle
     sid = oracle.build_seq_ids(lay.seg_frames, lay.seg_valid, lay.tokens_per_frame, lay.L)
+    ksid, Tk = None, None
+    if cl is not None:
+        Tk = cl.tokens_per_frame_k
+        ksid = oracle.build_seq_ids(lay.seg_frames, lay.seg_valid, Tk, cl.Lk)
     heads = list(range(budget_heads))
     t0 = time.perf_counter()
-    oracle.attention_fwd(tensors["q"], tensors["k"], tensors["v"], sid, heads=heads)
-    oracle.attention_bwd(tensors["q"], tensors["k"], tensors["v"], tensors["do"], sid, heads=heads)
+    oracle.attention_fwd(tensors["q"], tensors["k"], tensors["v"], sid, heads=heads, k_seq_id=ksid)
+    oracle.attention_bwd(tensors["q"], tensors["k"], tensors["v"], tensors["do"], sid, heads=heads, k_seq_id=ksid)
     dt = time.perf_counter() - t0
-    flops = (FLOPS_PER_PAIR_FWD + FLOPS_PER_PAIR_BWD) * lay.D * len(heads) * unmasked_pairs(lay)
+    flops = (FLOPS_PER_PAIR_FWD + FLOPS_PER_PAIR_BWD) * lay.D * len(heads) * unmasked_pairs(lay, Tk)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": f"fp64 numpy oracle, fwd+bwd of {len(heads)} of {lay.H} heads over all {lay.K} episodes "
                       f"({lay.L} tokens), {dt:.1f} s; BLAS threads = host cores"}
@@ -196,35 +213,44 @@ def run_gpu(args):
     import workloads as wl
 
     rank, world, local = dist_setup(args.gpus)
-    lay = wl.config_layout(WORKLOADS[args.workload])
-    host = wl.make_tensors(lay)  # bf16 CPU tensors, seeded
+    number, cross = WORKLOADS[args.workload]
+    cl = wl.cross_config_layout(number) if cross else None
+    lay = cl.q if cross else wl.config_layout(number)
+    host = wl.make_cross_tensors(cl) if cross else wl.make_tensors(lay)  # bf16 CPU tensors, seeded
     dev = {k: v.cuda() for k, v in host.items()}
     B, L, H, D = lay.B, lay.L, lay.H, lay.D
     T = lay.tokens_per_frame
-    pairs = unmasked_pairs(lay)
+    Tk, Lk = (cl.tokens_per_frame_k, cl.Lk) if cross else (T, L)
+    pairs = unmasked_pairs(lay, Tk)
     valid_tokens = int(lay.seg_valid.sum()) * T
+    launches = LAUNCHES_PER_STEP + (1 if cross else 0)
     flops_fwd = FLOPS_PER_PAIR_FWD * D * H * pairs
     flops_bwd = FLOPS_PER_PAIR_BWD * D * H * pairs
     flops = flops_fwd + flops_bwd
 
     sid = torch.empty((B, L), dtype=torch.int32, device="cuda")
-    tm_ws = torch.empty(pvl.tile_map_ws_bytes(B, L), dtype=torch.uint8, device="cuda")
+    ksid = torch.empty((B, Lk), dtype=torch.int32, device="cuda") if cross else None
+    tm_ws = torch.empty(pvl.tile_map_ws_bytes(B, L, Lk=Lk), dtype=torch.uint8, device="cuda")
     o = torch.empty_like(dev["q"])
     lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
-    dq, dk, dv = (torch.empty_like(dev["q"]) for _ in range(3))
-    bws = torch.empty(pvl.masked_attn_bwd_ws_bytes(B, L, H, D), dtype=torch.uint8, device="cuda")
+    dq = torch.empty_like(dev["q"])
+    dk, dv = (torch.empty_like(dev["k"]) for _ in range(2))
+    bws = torch.empty(pvl.masked_attn_bwd_ws_bytes(B, L, H, D, Lk=Lk), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
     def step(timers=None):
         pvl.pack_build_seq_ids(lay.seg_frames, lay.seg_valid, T, L, out=sid)
-        tm = pvl.tile_map_build(sid, ws=tm_ws)
+        if cross:
+            pvl.pack_build_seq_ids(lay.seg_frames, lay.seg_valid, Tk, Lk, out=ksid)
+        tm = pvl.tile_map_build(sid, ws=tm_ws, k_seq_id=ksid)
         if timers is not None:
             timers[0].record(stream)
-        pvl.masked_attn_fwd(dev["q"], dev["k"], dev["v"], sid, tm, o=o, lse=lse)
+        pvl.masked_attn_fwd(dev["q"], dev["k"], dev["v"], sid, tm, o=o, lse=lse, k_seq_id=ksid)
         if timers is not None:
             timers[1].record(stream)
-        pvl.masked_attn_bwd(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, sid, tm, dq=dq, dk=dk, dv=dv, ws=bws)
+        pvl.masked_attn_bwd(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, sid, tm, dq=dq, dk=dk, dv=dv, ws=bws,
+                            k_seq_id=ksid)
         if timers is not None:
             timers[2].record(stream)
 
@@ -283,7 +309,7 @@ def run_gpu(args):
 
     # tile efficiency: unmasked pairs / pairs inside the tiles the kernels
     # compute (FULL + PARTIAL), forward on 256 x 128 tiles, backward on 128 x 128
-    tmh = pvl.tile_map_build(sid, ws=tm_ws)
+    tmh = pvl.tile_map_build(sid, ws=tm_ws, k_seq_id=ksid)
     tile_eff = {}
     for name, level, area in (("fwd", 1, 256 * 128), ("bwd", 0, 128 * 128)):
         cls = tmh.to_host(level)["cls"]
@@ -293,7 +319,7 @@ def run_gpu(args):
     peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
     value = world * flops / (ms_step * 1e-3) / 1e12
     bwd_achieved = flops_bwd / (bwd_ms * 1e-3) / 1e12
-    traffic = traffic_record("attn_bwd.cu")
+    traffic = traffic_record("attn_bwd.cu", args.workload)
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -308,12 +334,14 @@ def run_gpu(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": describe(lay, valid_tokens),
+            "workload": describe(lay, valid_tokens, cl),
             "B": B, "L": L, "H": H, "D": D, "tokens_per_frame": T,
+            **({"Lk": Lk, "tokens_per_frame_k": Tk} if cross else {}),
             "unmasked_pairs_per_head": pairs,
             "tile_efficiency": tile_eff,
             "step": "pack_build_seq_ids + tile_map_build + masked_attn_fwd + masked_attn_bwd",
-            "l2": f"inputs larger than L2 (Q, K, V, dO are {dev['q'].numel() * 2 / 1e6:.0f} MB each); no flush",
+            "l2": (f"inputs larger than L2 (Q, dO {dev['q'].numel() * 2 / 1e6:.0f} MB each, K, V "
+                   f"{dev['k'].numel() * 2 / 1e6:.0f} MB each); no flush"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "tokens_per_s": round(world * valid_tokens / (ms_step * 1e-3), 1),
@@ -328,7 +356,7 @@ def run_gpu(args):
         "clocks": clk,
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": launches * args.steps,
         "roofline": {
             "kernel": "masked_attn_bwd (bwd_pre + bwd_main + bwd_convert launches, timed together)",
             "bound": "tensor", "achieved": round(bwd_achieved, 2), "peak": peak, "unit": "TFLOP/s",
@@ -338,7 +366,7 @@ def run_gpu(args):
         },
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(lay, host)
+        result["cpu_baseline"] = cpu_baseline(lay, host, cl=cl)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
