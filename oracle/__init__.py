@@ -19,12 +19,17 @@ What it computes, written from the LingBot-VA packing reports:
   in which query i attends key j iff seq_id[i] == seq_id[j] >= 0, and its
   analytic gradient ("furniture_packing_variable_length", the seq_id = -1
   masking paragraph; "lingbot_va_attn_profiling", doc_id[q] == doc_id[k]).
+- ``adaln.adaln_fwd`` / ``adaln.adaln_bwd``: layer norm over the feature
+  dimension followed by the AdaLN modulation y = xh (1 + scale) + shift, and
+  its gradient with the modulation gradients summed over the sequence
+  ("AdaptiveLoad" §2.B, the fused LayerNorm-Modulate kernel).
 
 Every function is pinned by tests under ``tests/`` against brute force,
 finite differences, closed forms, library routines (torch fp64 autograd and
 scaled_dot_product_attention) and the pages' packed == separate invariant.
 """
 
+from .adaln import adaln_bwd, adaln_fwd  # noqa: F401
 from .attention import attention_bwd, attention_fwd, effective_pairs  # noqa: F401
 from .seq_ids import build_seq_ids  # noqa: F401
 from .tile_map import EMPTY, FULL, PARTIAL, build_tile_map, tile_stats  # noqa: F401
