@@ -263,6 +263,38 @@ PVL_API pvl_status masked_attn_bwd_no_alloc(const pvl_bf16* q, const pvl_bf16* k
                                             pvl_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * adaln_fwd / adaln_bwd — layer norm over the feature dimension followed by
+ * the AdaLN modulation, fused ("AdaptiveLoad" §2.B, the fused
+ * LayerNorm-Modulate kernel of a DiT / MMDiT block; the page gives no
+ * formulas, the plain reading is the adaptive layer norm of DiT):
+ *   mu = mean_d x,  r = 1 / sqrt(mean_d (x - mu)^2 + eps),
+ *   y = (x - mu) r (1 + scale_b) + shift_b           (no affine of its own)
+ *   backward, g = dy (1 + scale_b), xh = (x - mu) r:
+ *   dx = r (g - mean_d g - xh mean_d(g xh)),
+ *   dshift_b = sum_n dy,  dscale_b = sum_n dy xh.
+ *
+ * x, y, dy, dx: dev bf16 [B, N, D]; shift, scale, dshift, dscale: dev fp32
+ * [B, D] (one modulation vector per batch row, shared by its N tokens).
+ * D a multiple of 8, at most 8192; eps >= 0 (1e-6 is the usual choice).
+ * mean, rstd: optional (null allowed) dev fp32 [B, N] row statistics the
+ * forward can write; the backward recomputes them from x and needs neither.
+ * adaln_bwd ws: dev scratch of adaln_bwd_ws_bytes(B, N, D) bytes (per-tile
+ * partial sums of dshift / dscale); contents on entry are ignored.
+ * All pointers 16-byte aligned (mean / rstd 4-byte).  Errors: INVALID_ARG
+ * for null pointers, sizes < 1, a negative eps or a short workspace;
+ * UNSUPPORTED for other D or misaligned pointers; CUDA for launch failures;
+ * a device-side bounded wait that runs out surfaces through pvl_device_error.
+ * ---------------------------------------------------------------------- */
+PVL_API pvl_status adaln_fwd(const pvl_bf16* x, const float* shift, const float* scale, int B, int N, int D,
+                             float eps, pvl_bf16* y, float* mean, float* rstd, pvl_stream_t stream);
+
+PVL_API size_t adaln_bwd_ws_bytes(int B, int N, int D);
+
+PVL_API pvl_status adaln_bwd(const pvl_bf16* x, const float* scale, const pvl_bf16* dy, int B, int N, int D,
+                             float eps, pvl_bf16* dx, float* dshift, float* dscale, void* ws, size_t ws_bytes,
+                             pvl_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Device error record.  Synchronises `stream`, reads and clears the current
  * device's error record.  Returns PVL_OK, PVL_ERR_TIMEOUT (a bounded wait ran
  * out; the kernel released its resources and returned), PVL_ERR_INVALID_ARG

@@ -13,6 +13,9 @@ from .api import (  # noqa: F401
     PARTIAL,
     PvlError,
     TileMap,
+    adaln_bwd,
+    adaln_bwd_ws_bytes,
+    adaln_fwd,
     device_error,
     masked_attn_bwd,
     masked_attn_bwd_no_alloc,
@@ -23,4 +26,4 @@ from .api import (  # noqa: F401
     tile_map_ws_bytes,
     version,
 )
-from .autograd import packed_attention  # noqa: F401
+from .autograd import adaln_modulate, packed_attention  # noqa: F401

@@ -36,6 +36,9 @@ SIGNATURES = {
     "masked_attn_bwd_ws_bytes_cross": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "masked_attn_bwd_cross": (_c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int, _c_int,
                                        _c_float, _p, _p, _p, _p, _c_size, _p]),
+    "adaln_fwd": (_c_int, [_p, _p, _p, _c_int, _c_int, _c_int, _c_float, _p, _p, _p, _p]),
+    "adaln_bwd_ws_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "adaln_bwd": (_c_int, [_p, _p, _p, _c_int, _c_int, _c_int, _c_float, _p, _p, _p, _p, _c_size, _p]),
     "pvl_device_error": (_c_int, [_p]),
     "pvl_device_error_detail": (_c_int, [_p, _p]),
     "pvl_last_error_message": (ctypes.c_char_p, []),

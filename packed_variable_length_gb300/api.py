@@ -295,6 +295,57 @@ def masked_attn_bwd_no_alloc(q, k, v, o, do, lse, seq_id, tile_map: TileMap, sca
     return dq, dk, dv
 
 
+# -------------------------------------------------------------------- AdaLN
+def adaln_fwd(x, shift, scale, eps: float = 1e-6, y=None, stats: bool = False, stream=None):
+    """y = layer_norm(x) * (1 + scale) + shift ("AdaptiveLoad" §2.B): x bf16
+    [B, N, D], shift / scale fp32 [B, D].  Returns y, or (y, mean, rstd) with
+    stats=True."""
+    if x.dim() != 3:
+        raise ValueError("x must be [B, N, D]")
+    B, N, D = x.shape
+    _need_cuda(x, "x", torch.bfloat16, (B, N, D))
+    _need_cuda(shift, "shift", torch.float32, (B, D))
+    _need_cuda(scale, "scale", torch.float32, (B, D))
+    y = torch.empty_like(x) if y is None else y
+    _need_cuda(y, "y", torch.bfloat16, (B, N, D))
+    mean = rstd = None
+    if stats:
+        mean = torch.empty((B, N), dtype=torch.float32, device=x.device)
+        rstd = torch.empty((B, N), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        _check(_lib.load().adaln_fwd(x.data_ptr(), shift.data_ptr(), scale.data_ptr(), B, N, D, float(eps),
+                                     y.data_ptr(), _ptr(mean), _ptr(rstd), _stream(stream)))
+    return (y, mean, rstd) if stats else y
+
+
+def adaln_bwd_ws_bytes(B: int, N: int, D: int) -> int:
+    return int(_lib.load().adaln_bwd_ws_bytes(B, N, D))
+
+
+def adaln_bwd(x, scale, dy, eps: float = 1e-6, dx=None, dshift=None, dscale=None, ws=None, stream=None):
+    """(dx bf16 [B, N, D], dshift fp32 [B, D], dscale fp32 [B, D]) of adaln_fwd."""
+    if x.dim() != 3:
+        raise ValueError("x must be [B, N, D]")
+    B, N, D = x.shape
+    _need_cuda(x, "x", torch.bfloat16, (B, N, D))
+    _need_cuda(dy, "dy", torch.bfloat16, (B, N, D))
+    _need_cuda(scale, "scale", torch.float32, (B, D))
+    dx = torch.empty_like(x) if dx is None else dx
+    dshift = torch.empty((B, D), dtype=torch.float32, device=x.device) if dshift is None else dshift
+    dscale = torch.empty((B, D), dtype=torch.float32, device=x.device) if dscale is None else dscale
+    _need_cuda(dx, "dx", torch.bfloat16, (B, N, D))
+    _need_cuda(dshift, "dshift", torch.float32, (B, D))
+    _need_cuda(dscale, "dscale", torch.float32, (B, D))
+    lib = _lib.load()
+    nbytes = int(lib.adaln_bwd_ws_bytes(B, N, D))
+    if ws is None:
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        _check(lib.adaln_bwd(x.data_ptr(), scale.data_ptr(), dy.data_ptr(), B, N, D, float(eps), dx.data_ptr(),
+                             dshift.data_ptr(), dscale.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return dx, dshift, dscale
+
+
 # ------------------------------------------------------------------- errors
 def device_error(stream=None, raise_on_error: bool = True):
     """Synchronises the stream and returns (status, [code, where, block, thread])."""

@@ -36,3 +36,25 @@ def packed_attention(q, k, v, seq_id, tile_map=None, scale=None, k_seq_id=None):
     if tile_map is None:
         tile_map = api.tile_map_build(seq_id, k_seq_id=k_seq_id)
     return _PackedAttention.apply(q, k, v, seq_id, k_seq_id, tile_map, scale)
+
+
+class _AdaLNModulate(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, shift, scale, eps):
+        y = api.adaln_fwd(x, shift, scale, eps)
+        ctx.save_for_backward(x, scale)
+        ctx.eps = eps
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, scale = ctx.saved_tensors
+        dx, dshift, dscale = api.adaln_bwd(x, scale, dy.contiguous(), ctx.eps)
+        return dx, dshift, dscale, None
+
+
+def adaln_modulate(x, shift, scale, eps: float = 1e-6):
+    """layer_norm(x) * (1 + scale) + shift over bf16 x [B, N, D] with fp32
+    shift / scale [B, D], differentiable ("AdaptiveLoad" §2.B); the backward
+    recomputes the row statistics from x."""
+    return _AdaLNModulate.apply(x, shift, scale, eps)

@@ -48,7 +48,7 @@ def test_only_declared_symbols_are_exported(lib):
     if out.returncode != 0:
         pytest.skip("nm unavailable")
     names = {ln.split()[-1] for ln in out.stdout.splitlines() if " T " in ln}
-    ours = {n for n in names if n.startswith(("pvl_", "pack_", "tile_map", "masked_attn"))}
+    ours = {n for n in names if n.startswith(("pvl_", "pack_", "tile_map", "masked_attn", "adaln_"))}
     assert ours == set(declared_symbols())
 
 
@@ -68,6 +68,18 @@ def test_host_validation_without_gpu(lib):
                                dummy, dummy, dummy, dummy, 0, null) == 1   # short workspace
     assert lib.tile_map_build(null, 1, 1, 128, 128, null, 0, null) == 1
     assert lib.tile_map_ws_bytes(0, 10, 128, 128) == 0
+    # cross attention: key length checked on its own side
+    assert lib.masked_attn_fwd_cross(dummy, dummy, dummy, dummy, dummy, dummy, 1, 128, 0, 1, 64, 0.1, dummy,
+                                     dummy, null) == 1
+    assert lib.tile_map_build_cross(dummy, null, 1, 10, 10, 128, 128, dummy, 1 << 20, null) == 1
+    assert lib.tile_map_ws_bytes_cross(1, 10, 0, 128, 128) == 0
+    assert lib.tile_map_ws_bytes_cross(2, 1000, 300, 128, 128) < lib.tile_map_ws_bytes(2, 1000, 128, 128)
+    # AdaLN: D must be a multiple of 8 up to 8192; eps >= 0; workspace size
+    assert lib.adaln_fwd(dummy, dummy, dummy, 1, 4, 100, 1e-6, dummy, null, null, null) == 2
+    assert lib.adaln_fwd(dummy, dummy, dummy, 1, 4, 8200, 1e-6, dummy, null, null, null) == 2
+    assert lib.adaln_fwd(dummy, dummy, dummy, 1, 4, 64, -1.0, dummy, null, null, null) == 1
+    assert lib.adaln_bwd(dummy, dummy, dummy, 1, 4, 64, 1e-6, dummy, dummy, dummy, dummy, 0, null) == 1
+    assert lib.adaln_bwd_ws_bytes(2, 100, 64) == 2 * 2 * 2 * 64 * 4   # two 64-token tiles per row
 
 
 def test_tile_map_layout_host(lib):
