@@ -374,6 +374,134 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------ AdaLN workload
+ADALN_SHAPE = (1, 64000, 5120)  # B, N (the page's 64k sequence), D (a 14B-class DiT width)
+
+
+def run_adaln(args):
+    """Fused LayerNorm-Modulate forward + backward ("AdaptiveLoad" §2.B) at
+    B = 1, N = 64,000, D = 5120; HBM bound, so the metric is algorithmic
+    bytes per second: forward reads x and writes y (4 N D bytes plus the
+    modulation vectors), backward reads x and dy and writes dx (6 N D bytes
+    plus the modulation vectors and their gradients)."""
+    import torch
+    import packed_variable_length_gb300 as pvl
+
+    rank, world, local = dist_setup(args.gpus)
+    B, N, D = ADALN_SHAPE
+    g = torch.Generator().manual_seed(2605)
+    host = {"x": (torch.randn(B, N, D, generator=g) * 2).to(torch.bfloat16),
+            "dy": torch.randn(B, N, D, generator=g).to(torch.bfloat16),
+            "shift": torch.randn(B, D, generator=g), "scale": torch.randn(B, D, generator=g) * 0.3}
+    dev = {k: v.cuda() for k, v in host.items()}
+    y = torch.empty_like(dev["x"])
+    dx = torch.empty_like(dev["x"])
+    dshift = torch.empty(B, D, device="cuda")
+    dscale = torch.empty(B, D, device="cuda")
+    ws = torch.empty(pvl.adaln_bwd_ws_bytes(B, N, D), dtype=torch.uint8, device="cuda")
+    bytes_fwd = 4 * N * D * B + 8 * B * D
+    bytes_bwd = 6 * N * D * B + 12 * B * D
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(timers=None):
+        if timers is not None:
+            timers[0].record(stream)
+        pvl.adaln_fwd(dev["x"], dev["shift"], dev["scale"], 1e-6, y=y)
+        if timers is not None:
+            timers[1].record(stream)
+        pvl.adaln_bwd(dev["x"], dev["scale"], dev["dy"], 1e-6, dx=dx, dshift=dshift, dscale=dscale, ws=ws)
+        if timers is not None:
+            timers[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    pvl.device_error()
+    timers = [[ev(), ev(), ev()] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(timers[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    pvl.device_error()
+    ms_step = max_over_ranks(t0.elapsed_time(t1), world) / args.steps
+    fwd_ms = sum(t[0].elapsed_time(t[1]) for t in timers) / args.steps
+    bwd_ms = sum(t[1].elapsed_time(t[2]) for t in timers) / args.steps
+
+    pin = {k: v.pin_memory() for k, v in host.items()}
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("y", y), ("dx", dx), ("dshift", dshift), ("dscale", dscale))}
+
+    def e2e_step():
+        for k in host:
+            dev[k].copy_(pin[k], non_blocking=True)
+        step()
+        for n, t in (("y", y), ("dx", dx), ("dshift", dshift), ("dscale", dscale)):
+            out_host[n].copy_(t, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    pvl.device_error()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    peaks = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    value = world * (bytes_fwd + bytes_bwd) / (ms_step * 1e-3) / 1e9
+    bwd_gbs = bytes_bwd / (bwd_ms * 1e-3) / 1e9
+    result = {
+        "metric": "fused LayerNorm-Modulate fwd+bwd algorithmic GB/s and tokens/s at 1 GB300",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in/out, fp32 arithmetic", "data": "synthetic",
+        "config": {"workload": f"adaln64k: B = {B}, N = {N}, D = {D}, x ~ N(0, 4), scale ~ N(0, 0.09), shift ~ N(0, 1)",
+                   "B": B, "N": N, "D": D, "l2": "x, y, dy, dx are 655 MB each (larger than L2); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_per_s": round(world * B * N / (ms_step * 1e-3), 1),
+        "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
+        "fwd_gbs": round(bytes_fwd / (fwd_ms * 1e-3) / 1e9, 1), "bwd_gbs": round(bwd_gbs, 1),
+        "clocks": clk,
+        "e2e": {"value": round(world * (bytes_fwd + bytes_bwd) / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in pin.values()),
+                "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in out_host.values())},
+        "gpu_launches": 3 * args.steps,
+        "roofline": {"kernel": "adaln_bwd (row kernel + tile-sum kernel, timed together)", "bound": "hbm",
+                     "achieved": round(bwd_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(bwd_gbs / hbm, 4),
+                     "traffic": None, "peak_note": f"of {peaks['source']} (STREAM-style copy)",
+                     "algorithmic": "6 N D + 12 B D bytes per launch"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n = 2000
+        t = time.perf_counter()
+        oracle.adaln_fwd(host["x"][:, :n], host["shift"], host["scale"])
+        oracle.adaln_bwd(host["x"][:, :n], host["shift"], host["scale"], host["dy"][:, :n])
+        dt = time.perf_counter() - t
+        result["cpu_baseline"] = {"value": round((10 * n * D * B) / dt / 1e9, 3), "unit": "GB/s",
+                                  "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                                  "sample": f"fp64 numpy oracle, fwd+bwd of the first {n} of {N} tokens, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ----------------------------------------------------------- reference arm
 def run_reference(args):
     """The fp64 oracle on the host cores, one bounded sample per step: fwd + bwd
@@ -424,7 +552,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="concat64k", choices=sorted(WORKLOADS),
+    ap.add_argument("--workload", default="concat64k", choices=sorted(WORKLOADS) + ["adaln64k"],
                     help="concat64k is the headline workload; the others are smaller cases for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -432,6 +560,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "adaln64k":
+        run_adaln(args)
     else:
         run_gpu(args)
 

@@ -45,12 +45,6 @@ enum AdalnSite : uint32_t { kSiteRowFull = 41 };
 // Stage bytes of one row of D bf16, rounded up to 128 bytes.
 __host__ __device__ constexpr int row_bytes(int D) { return ((D * 2 + 127) / 128) * 128; }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 __device__ __forceinline__ float2 warp_sum2(float2 v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -75,13 +69,21 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
   return t;
 }
 
-__device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
+// 8 fp32 values as 4 pairs from global memory through the read-only cache
+__device__ __forceinline__ void load_scale(const float* p8, float2 (&v)[4]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p8));
+  const float4 c = __ldg(reinterpret_cast<const float4*>(p8) + 1);
+  v[0] = make_float2(a.x, a.y);
+  v[1] = make_float2(a.z, a.w);
+  v[2] = make_float2(c.x, c.y);
+  v[3] = make_float2(c.z, c.w);
+}
+
+// 8 bf16 values (one 16-byte vector) as 4 fp32 pairs, in order
+__device__ __forceinline__ void unpack8x2(const uint4 u, float2 (&f)[4]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
+  for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
 }
 
 struct AdalnParams {
@@ -100,13 +102,18 @@ struct AdalnParams {
   uint64_t timeout_ns;
 };
 
-// Row `i` of this CTA's sequence of rows: forward row index, or (backward)
-// the token of work item `item` at offset `k`.
+// CTAs per SM: two, except the widest backward rows (registers).
+template <int kV, bool kBwd>
+constexpr int ctas_per_sm() {
+  return (kBwd && kV == 4) ? 1 : 2;
+}
+
 template <int kV, bool kBwd, int kStages>
-__global__ void __launch_bounds__(kThreads, 1) adaln_kernel(const AdalnParams p) {
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<kV, kBwd>()) adaln_kernel(const AdalnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full[kStages];
-  __shared__ float2 red[3][kWarps];
+  __shared__ float2 red_m[kWarps];  // row statistics
+  __shared__ float2 red[kWarps];    // backward: sums of g and g xh
   __shared__ int abort_s;
   constexpr int kTensors = kBwd ? 2 : 1;
   const int D = p.D;
@@ -162,38 +169,31 @@ __global__ void __launch_bounds__(kThreads, 1) adaln_kernel(const AdalnParams p)
   bool alive = true;
   // per-thread modulation of the owned feature groups, reloaded when the
   // batch row changes
-  float mod[kV][8];  // 1 + scale
-  float sh[kV][8];   // shift (forward)
+  float2 mod[kV][4];  // 1 + scale (forward)
+  float2 sh[kV][4];   // shift (forward)
   int cur_b = -1;
   for (long long item = blockIdx.x; item < p.items && alive; item += gridDim.x) {
     const int nrows = item_rows(item);
     const int b = static_cast<int>(row_index(item, 0) / p.N);
-    float acc_s[kBwd ? kV : 1][8], acc_c[kBwd ? kV : 1][8];  // dshift, dscale partials
-    const bool reload = b != cur_b;
+    float2 acc_s[kBwd ? kV : 1][4], acc_c[kBwd ? kV : 1][4];  // dshift, dscale partials
+    const bool reload = !kBwd && b != cur_b;
     cur_b = b;
 #pragma unroll
     for (int i = 0; i < kV; ++i) {
       if (kBwd) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc_s[i][e] = acc_c[i][e] = 0.0f;
+        for (int e = 0; e < 4; ++e) acc_s[i][e] = acc_c[i][e] = make_float2(0.f, 0.f);
       }
       if (!reload) continue;
       const int v = t + i * kThreads;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        mod[i][e] = 1.0f;
-        sh[i][e] = 0.0f;
-      }
       if (v < nvec) {
-        const float4* sc = reinterpret_cast<const float4*>(p.scale + static_cast<size_t>(b) * D + v * 8);
-        const float4 c0 = __ldg(sc), c1 = __ldg(sc + 1);
-        mod[i][0] = 1.0f + c0.x; mod[i][1] = 1.0f + c0.y; mod[i][2] = 1.0f + c0.z; mod[i][3] = 1.0f + c0.w;
-        mod[i][4] = 1.0f + c1.x; mod[i][5] = 1.0f + c1.y; mod[i][6] = 1.0f + c1.z; mod[i][7] = 1.0f + c1.w;
-        if (!kBwd) {
-          const float4* sf = reinterpret_cast<const float4*>(p.shift + static_cast<size_t>(b) * D + v * 8);
-          const float4 s0 = __ldg(sf), s1 = __ldg(sf + 1);
-          sh[i][0] = s0.x; sh[i][1] = s0.y; sh[i][2] = s0.z; sh[i][3] = s0.w;
-          sh[i][4] = s1.x; sh[i][5] = s1.y; sh[i][6] = s1.z; sh[i][7] = s1.w;
+        float2 sc[4], sf[4];
+        load_scale(p.scale + static_cast<size_t>(b) * D + v * 8, sc);
+        load_scale(p.shift + static_cast<size_t>(b) * D + v * 8, sf);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          mod[i][e] = make_float2(1.0f + sc[e].x, 1.0f + sc[e].y);
+          sh[i][e] = sf[e];
         }
       }
     }
@@ -205,33 +205,34 @@ __global__ void __launch_bounds__(kThreads, 1) adaln_kernel(const AdalnParams p)
       }
       const uint8_t* src = smem + static_cast<size_t>(st) * kTensors * RB;
       const long long r = row_index(item, k);
-      float xv[kV][8];
-      float s1 = 0.0f;
+      // Row statistics in one reduction of shifted sums: with K the row's
+      // first element, S1 = sum (x - K), S2 = sum (x - K)^2, mean = K + S1/D
+      // and var = S2/D - (S1/D)^2.  K is a sample of the row, so (mean - K)^2
+      // stays within a factor ~D of the variance even for an outlier K: the
+      // cancellation costs at most ~D * 2^-24 relative, far below bf16's 2^-9.
+      const float K = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(src)) << 16);
+      const float2 nk = make_float2(-K, -K);
+      float2 xv[kV][4];
+      float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < kV; ++i) {
         const int v = t + i * kThreads;
         if (v < nvec) {
-          unpack8(reinterpret_cast<const uint4*>(src)[v], xv[i]);
+          unpack8x2(reinterpret_cast<const uint4*>(src)[v], xv[i]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) s1 += xv[i][e];
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) xv[i][e] = 0.0f;
-        }
-      }
-      const float mu = block_sum2(make_float2(s1, 0.0f), red[0]).x / D;
-      float s2 = 0.0f;
-#pragma unroll
-      for (int i = 0; i < kV; ++i) {
-        if (t + i * kThreads < nvec) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float c = xv[i][e] - mu;
-            s2 = fmaf(c, c, s2);
+          for (int e = 0; e < 4; ++e) {
+            const float2 d = fadd2(xv[i][e], nk);
+            s1 = fadd2(s1, d);
+            s2 = ffma2(d, d, s2);
           }
         }
       }
-      const float rs = rsqrtf(block_sum2(make_float2(s2, 0.0f), red[1]).x / D + p.eps);
+      const float2 sums = block_sum2(make_float2(s1.x + s1.y, s2.x + s2.y), red_m);
+      const float m1 = sums.x / D;
+      const float mu = K + m1;
+      const float rs = rsqrtf(fmaxf(fmaf(-m1, m1, sums.y / D), 0.0f) + p.eps);
+      const float2 rs2 = make_float2(rs, rs);
+      const float2 nmu = make_float2(-mu, -mu);  // (x - mu) r: exactly 0 where x equals the mean
       if (!kBwd) {
 #pragma unroll
         for (int i = 0; i < kV; ++i) {
@@ -241,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1) adaln_kernel(const AdalnParams p)
             uint32_t* w = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float y0 = fmaf((xv[i][2 * e] - mu) * rs, mod[i][2 * e], sh[i][2 * e]);
-              const float y1 = fmaf((xv[i][2 * e + 1] - mu) * rs, mod[i][2 * e + 1], sh[i][2 * e + 1]);
-              w[e] = pack_bf16x2(y0, y1);
+              const float2 xh = fmul2(fadd2(xv[i][e], nmu), rs2);
+              const float2 yy = ffma2(xh, mod[i][e], sh[i][e]);
+              w[e] = pack_bf16x2(yy.x, yy.y);
             }
             reinterpret_cast<uint4*>(p.out + r * D)[v] = o;
           }
@@ -253,39 +254,43 @@ __global__ void __launch_bounds__(kThreads, 1) adaln_kernel(const AdalnParams p)
           if (p.rstd) p.rstd[r] = rs;
         }
       } else {
-        float gv[kV][8];
-        float sg = 0.0f, sgx = 0.0f;
+        const float* scale_row = p.scale + static_cast<size_t>(b) * D;
+        float2 sg = make_float2(0.f, 0.f), sgx = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < kV; ++i) {
           const int v = t + i * kThreads;
           if (v < nvec) {
-            float dv[8];
-            unpack8(reinterpret_cast<const uint4*>(src + RB)[v], dv);
+            float2 dv[4], sc[4];
+            unpack8x2(reinterpret_cast<const uint4*>(src + RB)[v], dv);
+            load_scale(scale_row + v * 8, sc);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float xh = (xv[i][e] - mu) * rs;
+            for (int e = 0; e < 4; ++e) {
+              const float2 xh = fmul2(fadd2(xv[i][e], nmu), rs2);
               xv[i][e] = xh;
-              gv[i][e] = dv[e] * mod[i][e];
-              sg += gv[i][e];
-              sgx = fmaf(gv[i][e], xh, sgx);
-              acc_s[i][e] += dv[e];
-              acc_c[i][e] = fmaf(dv[e], xh, acc_c[i][e]);
+              const float2 gg = ffma2(dv[e], sc[e], dv[e]);  // dy (1 + scale)
+              sg = fadd2(sg, gg);
+              sgx = ffma2(gg, xh, sgx);
+              acc_s[i][e] = fadd2(acc_s[i][e], dv[e]);
+              acc_c[i][e] = ffma2(dv[e], xh, acc_c[i][e]);
             }
           }
         }
-        const float2 m = block_sum2(make_float2(sg, sgx), red[2]);
-        const float mg = m.x / D, mgx = m.y / D;
+        const float2 m = block_sum2(make_float2(sg.x + sg.y, sgx.x + sgx.y), red);
+        const float2 nmg = make_float2(-m.x / D, -m.x / D), nmgx = make_float2(-m.y / D, -m.y / D);
 #pragma unroll
         for (int i = 0; i < kV; ++i) {
           const int v = t + i * kThreads;
           if (v < nvec) {
+            float2 dv[4], sc[4];  // dy again from shared memory: g = dy (1 + scale)
+            unpack8x2(reinterpret_cast<const uint4*>(src + RB)[v], dv);
+            load_scale(scale_row + v * 8, sc);
             uint4 o;
             uint32_t* w = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float d0 = rs * (gv[i][2 * e] - mg - xv[i][2 * e] * mgx);
-              const float d1 = rs * (gv[i][2 * e + 1] - mg - xv[i][2 * e + 1] * mgx);
-              w[e] = pack_bf16x2(d0, d1);
+              const float2 gg = ffma2(dv[e], sc[e], dv[e]);
+              const float2 dd = fmul2(fadd2(ffma2(xv[i][e], nmgx, gg), nmg), rs2);
+              w[e] = pack_bf16x2(dd.x, dd.y);
             }
             reinterpret_cast<uint4*>(p.out + r * D)[v] = o;
           }
@@ -304,10 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1) adaln_kernel(const AdalnParams p)
       for (int i = 0; i < kV; ++i) {
         const int v = t + i * kThreads;
         if (v < nvec) {
-          reinterpret_cast<float4*>(ps + v * 8)[0] = make_float4(acc_s[i][0], acc_s[i][1], acc_s[i][2], acc_s[i][3]);
-          reinterpret_cast<float4*>(ps + v * 8)[1] = make_float4(acc_s[i][4], acc_s[i][5], acc_s[i][6], acc_s[i][7]);
-          reinterpret_cast<float4*>(pc + v * 8)[0] = make_float4(acc_c[i][0], acc_c[i][1], acc_c[i][2], acc_c[i][3]);
-          reinterpret_cast<float4*>(pc + v * 8)[1] = make_float4(acc_c[i][4], acc_c[i][5], acc_c[i][6], acc_c[i][7]);
+          reinterpret_cast<float4*>(ps + v * 8)[0] = make_float4(acc_s[i][0].x, acc_s[i][0].y, acc_s[i][1].x, acc_s[i][1].y);
+          reinterpret_cast<float4*>(ps + v * 8)[1] = make_float4(acc_s[i][2].x, acc_s[i][2].y, acc_s[i][3].x, acc_s[i][3].y);
+          reinterpret_cast<float4*>(pc + v * 8)[0] = make_float4(acc_c[i][0].x, acc_c[i][0].y, acc_c[i][1].x, acc_c[i][1].y);
+          reinterpret_cast<float4*>(pc + v * 8)[1] = make_float4(acc_c[i][2].x, acc_c[i][2].y, acc_c[i][3].x, acc_c[i][3].y);
         }
       }
     }
@@ -333,9 +338,11 @@ __global__ void __launch_bounds__(256) adaln_bwd_finalize(const float* __restric
   (is_scale ? dscale : dshift)[j] = s;
 }
 
+// stages per CTA: at most ~96 KB of shared memory with two CTAs per SM,
+// ~192 KB with one
 template <bool kBwd>
 constexpr int stages_for(int kV) {
-  return kBwd ? (kV <= 3 ? 4 : 3) : (kV <= 3 ? 6 : 4);
+  return kBwd ? (kV <= 2 ? 6 : (kV == 3 ? 4 : 6)) : (kV <= 3 ? 6 : 5);
 }
 
 template <int kV, bool kBwd>
@@ -347,7 +354,8 @@ pvl_status launch_rows(const AdalnParams& p, cudaStream_t s, const char* who) {
   if (st != PVL_OK) return st;
   const int sms = sm_count();
   if (sms <= 0) return fail(PVL_ERR_CUDA, "%s: no usable CUDA device", who);
-  const long long grid = p.items < sms ? p.items : sms;
+  const long long cap = static_cast<long long>(ctas_per_sm<kV, kBwd>()) * sms;
+  const long long grid = p.items < cap ? p.items : cap;
   adaln_kernel<kV, kBwd, kStages><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
   return check_cuda(cudaGetLastError(), who);
 }
