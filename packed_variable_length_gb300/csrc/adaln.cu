@@ -12,14 +12,17 @@
 // Design.  The path is HBM bound (2 bytes read and 2 written per element
 // forward, 4 read and 2 written backward), so everything is about keeping
 // bytes in flight and touching each element once:
-//   - one persistent CTA of 256 threads per SM walks rows; thread 0 streams
-//     the rows (x, and dy backward) into a ring of shared-memory stages with
-//     bulk asynchronous copies, so several rows are in flight without
-//     holding them in registers;
-//   - the CTA works on one row at a time: each thread owns the same 8-wide
-//     feature groups of every row; row sums go through a warp shuffle and a
-//     block reduction (two-level, as the page describes), and the statistics
-//     never leave the chip; the modulation is applied on the way out;
+//   - persistent CTAs walk rows, each sized to the row: its threads own the
+//     row's 8-wide feature groups evenly (one or two per thread, 320
+//     threads at D = 5120), as many CTAs per SM as registers allow; thread 0
+//     streams the rows (x, and dy backward) into a ring of shared-memory
+//     stages with bulk asynchronous copies, so several rows are in flight
+//     without holding them in registers;
+//   - the CTA works on one row at a time: each thread owns the same feature
+//     groups of every row; row sums go through a warp shuffle and a block
+//     reduction (two-level, as the page describes), and the statistics never
+//     leave the chip; the modulation is applied on the way out.  The barrier
+//     that opens a row also frees the previous row's stage;
 //   - backward, the rows of a work item (one batch row, a tile of
 //     kRowsPerTile tokens) accumulate dshift / dscale in the registers of
 //     the threads that own each feature: the sequence-direction reduction of
@@ -35,8 +38,9 @@
 namespace pvl {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kMaxThreads = 512;
+constexpr int kMaxWarps = kMaxThreads / 32;
+constexpr int kMaxStages = 8;
 constexpr int kRowsPerTile = 64;  // backward work item: tokens of one batch row
 constexpr int kMaxD = 8192;
 
@@ -45,28 +49,48 @@ enum AdalnSite : uint32_t { kSiteRowFull = 41 };
 // Stage bytes of one row of D bf16, rounded up to 128 bytes.
 __host__ __device__ constexpr int row_bytes(int D) { return ((D * 2 + 127) / 128) * 128; }
 
-__device__ __forceinline__ float2 warp_sum2(float2 v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+// CTA-wide sums of kN values (2 or 4), the same in every thread.  Inside a
+// warp the values are reduce-scattered (each halving step sends half of the
+// remaining values), so lane group q = lane / (32 / kN) ends with value q;
+// one lane per group stores it in red[warp * kN + q].  After the barrier
+// each warp reads the table with one lane per entry and sums over the warps
+// with xor shuffles.  `red` holds kMaxWarps * kN floats and is not written
+// again before every thread has passed the caller's next __syncthreads.
+// Every thread returns the same bits (the order of the additions is fixed).
+template <int kN>
+__device__ __forceinline__ void block_sum(float (&a)[kN], float* red, int nwarps) {
+  static_assert(kN == 2 || kN == 4, "2 or 4 values");
+  const int lane = threadIdx.x & 31;
+  float kept;
+  if (kN == 4) {
+    const bool hi = lane & 16;
+    float k0 = hi ? a[2] : a[0], k1 = hi ? a[3] : a[1];
+    const float s0 = hi ? a[0] : a[2], s1 = hi ? a[1] : a[3];
+    k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+    k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+    const bool h8 = lane & 8;
+    kept = h8 ? k1 : k0;
+    kept += __shfl_xor_sync(0xffffffffu, h8 ? k0 : k1, 8);
+  } else {
+    const bool hi = lane & 16;
+    kept = hi ? a[1] : a[0];
+    kept += __shfl_xor_sync(0xffffffffu, hi ? a[0] : a[1], 16);
+    kept += __shfl_xor_sync(0xffffffffu, kept, 8);
   }
-  return v;
-}
-
-// Sum over the CTA through `red` (kWarps slots, not reused before the next
-// __syncthreads of the caller).
-__device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
-  v = warp_sum2(v);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  kept += __shfl_xor_sync(0xffffffffu, kept, 4);
+  kept += __shfl_xor_sync(0xffffffffu, kept, 2);
+  kept += __shfl_xor_sync(0xffffffffu, kept, 1);
+  constexpr int kGroup = 32 / kN;
+  if ((lane & (kGroup - 1)) == 0) red[(threadIdx.x >> 5) * kN + lane / kGroup] = kept;
   __syncthreads();
-  float2 t = red[0];
+  // entry lane (and lane + 32) of the table: warp lane / kN, value lane % kN
+  const int n = nwarps * kN;
+  float t = lane < n ? red[lane] : 0.0f;
+  if (n > 32 && lane + 32 < n) t += red[lane + 32];
 #pragma unroll
-  for (int w = 1; w < kWarps; ++w) {
-    t.x += red[w].x;
-    t.y += red[w].y;
-  }
-  return t;
+  for (int o = kN; o < 32; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+#pragma unroll
+  for (int q = 0; q < kN; ++q) a[q] = __shfl_sync(0xffffffffu, t, q);
 }
 
 // 8 fp32 values as 4 pairs from global memory through the read-only cache
@@ -97,84 +121,104 @@ struct AdalnParams {
   float* part;              // backward: [2][B * n_tiles][D] tile partials
   DeviceError* err;
   int B, N, D, n_tiles;
+  int units;                // rows per batch row: N forward, n_tiles backward
   long long items;          // forward: rows; backward: B * n_tiles
+  int stages;               // shared-memory row stages, 2..kMaxStages
   float eps;
   uint64_t timeout_ns;
 };
 
-// CTAs per SM: two, except the widest backward rows (registers).
-template <int kV, bool kBwd>
-constexpr int ctas_per_sm() {
-  return (kBwd && kV == 4) ? 1 : 2;
+// Backward rows keep their values in registers between the two passes at
+// one or two feature groups per thread and re-read them from shared memory
+// at more (where the per-feature accumulators take the registers).
+template <int kV>
+__host__ __device__ constexpr bool holds_row() {
+  return kV <= 2;
 }
 
-template <int kV, bool kBwd, int kStages>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm<kV, kBwd>()) adaln_kernel(const AdalnParams p) {
+// Register budget per thread for kV feature groups per thread.
+template <int kV, bool kBwd>
+constexpr int max_regs() {
+  return kBwd ? (kV == 1 ? 64 : (kV == 2 ? 96 : 128)) : (kV == 1 ? 48 : (kV == 2 ? 64 : (kV == 3 ? 96 : 128)));
+}
+
+// One CTA walks its items (forward: rows blockIdx.x, blockIdx.x + gridDim.x,
+// ...; backward: tiles of kRowsPerTile tokens of one batch row) with every
+// thread owning feature groups t, t + blockDim.x, ... (kV of them at most).
+template <int kV, bool kBwd>
+__global__ void __maxnreg__((max_regs<kV, kBwd>())) adaln_kernel(const AdalnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t full[kStages];
-  __shared__ float2 red_m[kWarps];  // row statistics
-  __shared__ float2 red[kWarps];    // backward: sums of g and g xh
+  __shared__ uint64_t full[kMaxStages];
+  __shared__ float red[kMaxWarps * 4];
   __shared__ int abort_s;
   constexpr int kTensors = kBwd ? 2 : 1;
+  constexpr bool kHold = !kBwd || holds_row<kV>();
   const int D = p.D;
   const int RB = row_bytes(D);
   const int nvec = D / 8;
   const int t = threadIdx.x;
+  const int nthr = blockDim.x;
+  const int nwarps = nthr / 32;
+  const int S = p.stages;
+  const float inv_d = 1.0f / static_cast<float>(D);
   const KernelCtl ctl{p.err, &abort_s, p.timeout_ns};
 
   if (t == 0) {
     abort_s = 0;
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
     fence_barrier_init();
   }
   __syncthreads();
 
-  // The rows this CTA handles, in order: forward rows blockIdx.x,
-  // blockIdx.x + gridDim.x, ...; backward whole items, kRowsPerTile tokens
-  // each (fewer in the last tile of a batch row).
-  auto item_rows = [&](long long item) -> int {
-    if (!kBwd) return 1;
-    const int tile = static_cast<int>(item % p.n_tiles);
-    const int n0 = tile * kRowsPerTile;
-    return min(kRowsPerTile, p.N - n0);
+  // Item -> (batch row, unit): advanced incrementally, no divisions per row.
+  auto advance = [&](int& b, int& u) {
+    u += gridDim.x;
+    if (u >= p.units) {
+      b += u / p.units;
+      u %= p.units;
+    }
   };
-  auto row_index = [&](long long item, int k) -> long long {  // global row b * N + n
-    if (!kBwd) return item;
-    const long long b = item / p.n_tiles;
-    const int tile = static_cast<int>(item % p.n_tiles);
-    return b * p.N + static_cast<long long>(tile) * kRowsPerTile + k;
+  auto rows_of = [&](int u) -> int { return kBwd ? min(kRowsPerTile, p.N - u * kRowsPerTile) : 1; };
+  auto row0_of = [&](int b, int u) -> long long {
+    return static_cast<long long>(b) * p.N + (kBwd ? u * kRowsPerTile : u);
   };
-  // Producer state (thread 0): next (item, k) to load.
-  long long ld_item = blockIdx.x;
-  int ld_k = 0;
+
+  // Producer state (thread 0): the next row to load.
+  const int first_b = static_cast<int>(blockIdx.x / p.units), first_u = static_cast<int>(blockIdx.x % p.units);
+  int ld_b = first_b, ld_u = first_u, ld_k = 0;
   uint32_t ld_n = 0;  // rows issued
+  int ld_st = 0;
   auto issue_next = [&]() {
-    if (ld_item >= p.items) return;
-    const int st = ld_n % kStages;
-    const long long r = row_index(ld_item, ld_k);
-    uint8_t* dst = smem + static_cast<size_t>(st) * kTensors * RB;
-    mbar_arrive_expect_tx(&full[st], kTensors * D * 2);
-    bulk_load(dst, p.x + r * D, D * 2, &full[st]);
-    if (kBwd) bulk_load(dst + RB, p.dy + r * D, D * 2, &full[st]);
+    if (ld_b >= p.B) return;
+    const long long r = row0_of(ld_b, ld_u) + ld_k;
+    uint8_t* dst = smem + static_cast<size_t>(ld_st) * kTensors * RB;
+    mbar_arrive_expect_tx(&full[ld_st], kTensors * D * 2);
+    bulk_load(dst, p.x + r * D, D * 2, &full[ld_st]);
+    if (kBwd) bulk_load(dst + RB, p.dy + r * D, D * 2, &full[ld_st]);
     ++ld_n;
-    if (++ld_k == item_rows(ld_item)) {
+    if (++ld_st == S) ld_st = 0;
+    if (++ld_k == rows_of(ld_u)) {
       ld_k = 0;
-      ld_item += gridDim.x;
+      advance(ld_b, ld_u);
     }
   };
   if (t == 0)
-    for (int s = 0; s < kStages; ++s) issue_next();
+    for (int s = 0; s < S; ++s) issue_next();
 
   uint32_t use_n = 0;  // rows consumed
+  int use_st = 0;
+  uint32_t use_ph = 0;
   bool alive = true;
-  // per-thread modulation of the owned feature groups, reloaded when the
-  // batch row changes
-  float2 mod[kV][4];  // 1 + scale (forward)
-  float2 sh[kV][4];   // shift (forward)
+  // per-thread modulation of the owned feature groups (forward), reloaded
+  // when the batch row changes
+  float2 mod[kBwd ? 1 : kV][4];  // 1 + scale
+  float2 sh[kBwd ? 1 : kV][4];   // shift
   int cur_b = -1;
-  for (long long item = blockIdx.x; item < p.items && alive; item += gridDim.x) {
-    const int nrows = item_rows(item);
-    const int b = static_cast<int>(row_index(item, 0) / p.N);
+  int it_b = first_b, it_u = first_u;
+  for (; it_b < p.B && alive; advance(it_b, it_u)) {
+    const int b = it_b;
+    const int nrows = rows_of(it_u);
+    const long long row0 = row0_of(b, it_u);
     float2 acc_s[kBwd ? kV : 1][4], acc_c[kBwd ? kV : 1][4];  // dshift, dscale partials
     const bool reload = !kBwd && b != cur_b;
     cur_b = b;
@@ -183,190 +227,270 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kV, kBwd>()) adaln_kerne
       if (kBwd) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc_s[i][e] = acc_c[i][e] = make_float2(0.f, 0.f);
-      }
-      if (!reload) continue;
-      const int v = t + i * kThreads;
-      if (v < nvec) {
-        float2 sc[4], sf[4];
-        load_scale(p.scale + static_cast<size_t>(b) * D + v * 8, sc);
-        load_scale(p.shift + static_cast<size_t>(b) * D + v * 8, sf);
+      } else if (reload) {
+        const int v = t + i * nthr;
+        if (v < nvec) {
+          float2 sc[4], sf[4];
+          load_scale(p.scale + static_cast<size_t>(b) * D + v * 8, sc);
+          load_scale(p.shift + static_cast<size_t>(b) * D + v * 8, sf);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          mod[i][e] = make_float2(1.0f + sc[e].x, 1.0f + sc[e].y);
-          sh[i][e] = sf[e];
+          for (int e = 0; e < 4; ++e) {
+            mod[i][e] = make_float2(1.0f + sc[e].x, 1.0f + sc[e].y);
+            sh[i][e] = sf[e];
+          }
         }
       }
     }
-    for (int k = 0; k < nrows; ++k, ++use_n) {
-      const int st = use_n % kStages;
-      if (!__syncthreads_and(mbar_wait(&full[st], (use_n / kStages) & 1, ctl, kSiteRowFull))) {
+    const float* scale_row = p.scale + static_cast<size_t>(b) * D;
+    for (int k = 0; k < nrows; ++k) {
+      if (!__syncthreads_and(mbar_wait(&full[use_st], use_ph, ctl, kSiteRowFull))) {
         alive = false;
         break;
       }
-      const uint8_t* src = smem + static_cast<size_t>(st) * kTensors * RB;
-      const long long r = row_index(item, k);
-      // Row statistics in one reduction of shifted sums: with K the row's
-      // first element, S1 = sum (x - K), S2 = sum (x - K)^2, mean = K + S1/D
-      // and var = S2/D - (S1/D)^2.  K is a sample of the row, so (mean - K)^2
-      // stays within a factor ~D of the variance even for an outlier K: the
-      // cancellation costs at most ~D * 2^-24 relative, far below bf16's 2^-9.
+      // Every thread is past the previous row: its stage and the reduction
+      // table are free, so the stage is refilled now.
+      if (t == 0 && use_n > 0) issue_next();
+      const uint8_t* src = smem + static_cast<size_t>(use_st) * kTensors * RB;
+      const long long r = row0 + k;
+      // Row statistics from shifted sums: with K the row's first element and
+      // d = x - K, S1 = sum d, S2 = sum d^2, m1 = S1/D, mean = K + m1,
+      // var = S2/D - m1^2 and xh = (d - m1) r.  K is a sample of the row, so
+      // m1^2 stays within a factor ~D of the variance even for an outlier K:
+      // the cancellation costs at most ~D * 2^-24 relative, far below bf16's
+      // 2^-9.  d is exact (two bf16 values), so xh = 0 exactly where x equals
+      // the mean.  Backward, the same pass sums g = dy (1 + scale) and g d:
+      // sum g xh = r (sum g d - m1 sum g), one reduction per row.
       const float K = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(src)) << 16);
       const float2 nk = make_float2(-K, -K);
-      float2 xv[kV][4];
+      float2 xv[kHold ? kV : 1][4];  // d
+      float2 dv[kBwd && kHold ? kV : 1][4];
       float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+      float2 sg = make_float2(0.f, 0.f), sgd = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < kV; ++i) {
-        const int v = t + i * kThreads;
+        const int v = t + i * nthr;
         if (v < nvec) {
-          unpack8x2(reinterpret_cast<const uint4*>(src)[v], xv[i]);
+          float2 xr[4], dr[4], sc[4];
+          unpack8x2(reinterpret_cast<const uint4*>(src)[v], xr);
+          if (kBwd) {
+            unpack8x2(reinterpret_cast<const uint4*>(src + RB)[v], dr);
+            load_scale(scale_row + v * 8, sc);
+          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 d = fadd2(xv[i][e], nk);
+            const float2 d = fadd2(xr[e], nk);
             s1 = fadd2(s1, d);
             s2 = ffma2(d, d, s2);
+            if (kHold) xv[kHold ? i : 0][e] = d;
+            if (kBwd) {
+              const float2 g = ffma2(dr[e], sc[e], dr[e]);
+              sg = fadd2(sg, g);
+              sgd = ffma2(g, d, sgd);
+              acc_s[kBwd ? i : 0][e] = fadd2(acc_s[kBwd ? i : 0][e], dr[e]);
+              if (kHold) dv[kBwd && kHold ? i : 0][e] = dr[e];
+            }
           }
         }
       }
-      const float2 sums = block_sum2(make_float2(s1.x + s1.y, s2.x + s2.y), red_m);
-      const float m1 = sums.x / D;
-      const float mu = K + m1;
-      const float rs = rsqrtf(fmaxf(fmaf(-m1, m1, sums.y / D), 0.0f) + p.eps);
-      const float2 rs2 = make_float2(rs, rs);
-      const float2 nmu = make_float2(-mu, -mu);  // (x - mu) r: exactly 0 where x equals the mean
+      float m1, rs;
+      float a = 0.f, c = 0.f;  // backward: dx = g r + xh a + c
       if (!kBwd) {
-#pragma unroll
-        for (int i = 0; i < kV; ++i) {
-          const int v = t + i * kThreads;
-          if (v < nvec) {
-            uint4 o;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 xh = fmul2(fadd2(xv[i][e], nmu), rs2);
-              const float2 yy = ffma2(xh, mod[i][e], sh[i][e]);
-              w[e] = pack_bf16x2(yy.x, yy.y);
-            }
-            reinterpret_cast<uint4*>(p.out + r * D)[v] = o;
-          }
-        }
-        if (t == 0) {
-          if (p.mean) p.mean[r] = mu;
-          if (p.rstd) p.rstd[r] = rs;
-        }
+        float sums[2] = {s1.x + s1.y, s2.x + s2.y};
+        block_sum<2>(sums, red, nwarps);
+        m1 = sums[0] * inv_d;
+        rs = rsqrtf(fmaxf(fmaf(-m1, m1, sums[1] * inv_d), 0.0f) + p.eps);
       } else {
-        const float* scale_row = p.scale + static_cast<size_t>(b) * D;
-        float2 sg = make_float2(0.f, 0.f), sgx = make_float2(0.f, 0.f);
+        float sums[4] = {s1.x + s1.y, s2.x + s2.y, sg.x + sg.y, sgd.x + sgd.y};
+        block_sum<4>(sums, red, nwarps);
+        m1 = sums[0] * inv_d;
+        rs = rsqrtf(fmaxf(fmaf(-m1, m1, sums[1] * inv_d), 0.0f) + p.eps);
+        const float mean_g = sums[2] * inv_d;
+        const float mean_gxh = rs * fmaf(-m1, sums[2], sums[3]) * inv_d;
+        a = -rs * mean_gxh;
+        c = -rs * mean_g;
+      }
+      const float2 rs2 = make_float2(rs, rs);
+      const float2 nm1 = make_float2(-m1, -m1);
+      const float2 a2 = make_float2(a, a), c2 = make_float2(c, c);
 #pragma unroll
-        for (int i = 0; i < kV; ++i) {
-          const int v = t + i * kThreads;
-          if (v < nvec) {
-            float2 dv[4], sc[4];
-            unpack8x2(reinterpret_cast<const uint4*>(src + RB)[v], dv);
-            load_scale(scale_row + v * 8, sc);
+      for (int i = 0; i < kV; ++i) {
+        const int v = t + i * nthr;
+        if (v < nvec) {
+          float2 d[4], dr[4];
+          if (kHold) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 xh = fmul2(fadd2(xv[i][e], nmu), rs2);
-              xv[i][e] = xh;
-              const float2 gg = ffma2(dv[e], sc[e], dv[e]);  // dy (1 + scale)
-              sg = fadd2(sg, gg);
-              sgx = ffma2(gg, xh, sgx);
-              acc_s[i][e] = fadd2(acc_s[i][e], dv[e]);
-              acc_c[i][e] = ffma2(dv[e], xh, acc_c[i][e]);
+            for (int e = 0; e < 4; ++e) d[e] = xv[kHold ? i : 0][e];
+          } else {
+            unpack8x2(reinterpret_cast<const uint4*>(src)[v], d);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[e] = fadd2(d[e], nk);
+          }
+          if (kBwd) {
+            if (kHold) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) dr[e] = dv[kBwd && kHold ? i : 0][e];
+            } else {
+              unpack8x2(reinterpret_cast<const uint4*>(src + RB)[v], dr);
             }
           }
-        }
-        const float2 m = block_sum2(make_float2(sg.x + sg.y, sgx.x + sgx.y), red);
-        const float2 nmg = make_float2(-m.x / D, -m.x / D), nmgx = make_float2(-m.y / D, -m.y / D);
+          float2 sc[4];
+          if (kBwd) load_scale(scale_row + v * 8, sc);
+          uint4 o;
+          uint32_t* w = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-        for (int i = 0; i < kV; ++i) {
-          const int v = t + i * kThreads;
-          if (v < nvec) {
-            float2 dv[4], sc[4];  // dy again from shared memory: g = dy (1 + scale)
-            unpack8x2(reinterpret_cast<const uint4*>(src + RB)[v], dv);
-            load_scale(scale_row + v * 8, sc);
-            uint4 o;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 gg = ffma2(dv[e], sc[e], dv[e]);
-              const float2 dd = fmul2(fadd2(ffma2(xv[i][e], nmgx, gg), nmg), rs2);
-              w[e] = pack_bf16x2(dd.x, dd.y);
+          for (int e = 0; e < 4; ++e) {
+            const float2 xh = fmul2(fadd2(d[e], nm1), rs2);
+            float2 out;
+            if (!kBwd) {
+              out = ffma2(xh, mod[kBwd ? 0 : i][e], sh[kBwd ? 0 : i][e]);
+            } else {
+              const float2 g = ffma2(dr[e], sc[e], dr[e]);
+              out = ffma2(g, rs2, ffma2(xh, a2, c2));
+              acc_c[kBwd ? i : 0][e] = ffma2(dr[e], xh, acc_c[kBwd ? i : 0][e]);
             }
-            reinterpret_cast<uint4*>(p.out + r * D)[v] = o;
+            w[e] = pack_bf16x2(out.x, out.y);
           }
+          reinterpret_cast<uint4*>(p.out + r * D)[v] = o;
         }
       }
-      // every thread is done with this stage and with the reduction slots
-      __syncthreads();
-      if (t == 0) issue_next();
+      if (!kBwd && t == 0) {
+        if (p.mean) p.mean[r] = K + m1;
+        if (p.rstd) p.rstd[r] = rs;
+      }
+      ++use_n;
+      if (++use_st == S) {
+        use_st = 0;
+        use_ph ^= 1u;
+      }
     }
     if (!alive) break;
     if (kBwd) {
       // this item's partial modulation gradients, coalesced along the features
+      const long long item = static_cast<long long>(b) * p.units + it_u;
       float* ps = p.part + static_cast<size_t>(item) * D;
       float* pc = p.part + (static_cast<size_t>(p.items) + item) * D;
 #pragma unroll
       for (int i = 0; i < kV; ++i) {
-        const int v = t + i * kThreads;
+        const int v = t + i * nthr;
         if (v < nvec) {
-          reinterpret_cast<float4*>(ps + v * 8)[0] = make_float4(acc_s[i][0].x, acc_s[i][0].y, acc_s[i][1].x, acc_s[i][1].y);
-          reinterpret_cast<float4*>(ps + v * 8)[1] = make_float4(acc_s[i][2].x, acc_s[i][2].y, acc_s[i][3].x, acc_s[i][3].y);
-          reinterpret_cast<float4*>(pc + v * 8)[0] = make_float4(acc_c[i][0].x, acc_c[i][0].y, acc_c[i][1].x, acc_c[i][1].y);
-          reinterpret_cast<float4*>(pc + v * 8)[1] = make_float4(acc_c[i][2].x, acc_c[i][2].y, acc_c[i][3].x, acc_c[i][3].y);
+          const int j = kBwd ? i : 0;
+          reinterpret_cast<float4*>(ps + v * 8)[0] = make_float4(acc_s[j][0].x, acc_s[j][0].y, acc_s[j][1].x, acc_s[j][1].y);
+          reinterpret_cast<float4*>(ps + v * 8)[1] = make_float4(acc_s[j][2].x, acc_s[j][2].y, acc_s[j][3].x, acc_s[j][3].y);
+          reinterpret_cast<float4*>(pc + v * 8)[0] = make_float4(acc_c[j][0].x, acc_c[j][0].y, acc_c[j][1].x, acc_c[j][1].y);
+          reinterpret_cast<float4*>(pc + v * 8)[1] = make_float4(acc_c[j][2].x, acc_c[j][2].y, acc_c[j][3].x, acc_c[j][3].y);
         }
       }
     }
   }
   // copies still in flight land before the CTA leaves
+  __syncthreads();
   if (t == 0)
-    for (uint32_t n = use_n; n < ld_n; ++n) mbar_drain(&full[n % kStages], (n / kStages) & 1, 100000000ull);
+    for (uint32_t n = use_n; n < ld_n; ++n) mbar_drain(&full[n % S], (n / S) & 1, 100000000ull);
   __syncthreads();
 }
 
-// dshift[b, d] / dscale[b, d] = sum over the batch row's tiles, in tile order.
-__global__ void __launch_bounds__(256) adaln_bwd_finalize(const float* __restrict__ part, int B, int D, int n_tiles,
-                                                          float* __restrict__ dshift, float* __restrict__ dscale) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long bd = static_cast<long long>(B) * D;
-  if (i >= 2 * bd) return;
-  const bool is_scale = i >= bd;
-  const long long j = is_scale ? i - bd : i;
-  const int b = static_cast<int>(j / D), d = static_cast<int>(j % D);
+// dshift[b, d] / dscale[b, d] = sum over the batch row's tiles.  A CTA
+// (blockIdx.x: batch row, then dshift / dscale; blockIdx.y: feature block)
+// covers 128 features of one (batch row, output): lane l of warp w adds the
+// float4 at features 4l.. of tiles w, w + 8, w + 16, ... (four loads in
+// flight), then warp 0 adds the eight warps' sums in warp order.  The order
+// of every addition is fixed: the result is deterministic.
+constexpr int kFinThreads = 256;
+__global__ void __launch_bounds__(kFinThreads) adaln_bwd_finalize(const float* __restrict__ part, int B, int D,
+                                                                  int n_tiles, float* __restrict__ dshift,
+                                                                  float* __restrict__ dscale) {
+  __shared__ float4 acc[kFinThreads / 32][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int d = blockIdx.y * 128 + lane * 4;
+  const int b = static_cast<int>(blockIdx.x % B);
+  const bool is_scale = static_cast<int>(blockIdx.x) >= B;
   const float* src = part + (is_scale ? static_cast<size_t>(B) * n_tiles * D : 0) + static_cast<size_t>(b) * n_tiles * D + d;
-  float s = 0.0f;
-  for (int tl = 0; tl < n_tiles; ++tl) s += src[static_cast<size_t>(tl) * D];
-  (is_scale ? dscale : dshift)[j] = s;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (d < D) {
+    constexpr int kW = kFinThreads / 32;
+    int tl = w;
+    for (; tl + 3 * kW < n_tiles; tl += 4 * kW) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(tl + u * kW) * D));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        s.x += v[u].x;
+        s.y += v[u].y;
+        s.z += v[u].z;
+        s.w += v[u].w;
+      }
+    }
+    for (; tl < n_tiles; tl += kW) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(tl) * D));
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+  }
+  acc[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && d < D) {
+    float4 t = acc[0][lane];
+#pragma unroll
+    for (int i = 1; i < kFinThreads / 32; ++i) {
+      const float4 v = acc[i][lane];
+      t.x += v.x;
+      t.y += v.y;
+      t.z += v.z;
+      t.w += v.w;
+    }
+    float* dst = (is_scale ? dscale : dshift) + static_cast<size_t>(b) * D + d;
+    *reinterpret_cast<float4*>(dst) = t;
+  }
 }
 
-// stages per CTA: at most ~96 KB of shared memory with two CTAs per SM,
-// ~192 KB with one
-template <bool kBwd>
-constexpr int stages_for(int kV) {
-  return kBwd ? (kV <= 2 ? 6 : (kV == 3 ? 4 : 6)) : (kV <= 3 ? 6 : 5);
-}
-
+// Launch shape: the CTA's threads cover the row's 8-wide feature groups
+// evenly (kV groups per thread, rounded to whole warps); as many CTAs per SM
+// as registers allow; the shared memory of the SM split among them as row
+// stages (2 to kMaxStages).
 template <int kV, bool kBwd>
-pvl_status launch_rows(const AdalnParams& p, cudaStream_t s, const char* who) {
-  constexpr int kStages = stages_for<kBwd>(kV);
-  const int smem = kStages * (kBwd ? 2 : 1) * row_bytes(p.D);
-  pvl_status st = check_cuda(
-      cudaFuncSetAttribute(adaln_kernel<kV, kBwd, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem), who);
+pvl_status launch_rows(AdalnParams p, cudaStream_t s, const char* who) {
+  const int nvec = p.D / 8;
+  const int threads = ((nvec + kV - 1) / kV + 31) / 32 * 32;
+  const int stage_bytes = (kBwd ? 2 : 1) * row_bytes(p.D);
+  int dev = 0, sms = 0, smem_sm = 0;
+  pvl_status st = check_cuda(cudaGetDevice(&dev), who);
+  if (st == PVL_OK) st = check_cuda(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), who);
+  if (st == PVL_OK)
+    st = check_cuda(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev), who);
+  int occ = 0;
+  if (st == PVL_OK)
+    st = check_cuda(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, adaln_kernel<kV, kBwd>, threads, 0), who);
   if (st != PVL_OK) return st;
-  const int sms = sm_count();
-  if (sms <= 0) return fail(PVL_ERR_CUDA, "%s: no usable CUDA device", who);
-  const long long cap = static_cast<long long>(ctas_per_sm<kV, kBwd>()) * sms;
+  if (sms <= 0 || occ <= 0) return fail(PVL_ERR_CUDA, "%s: no usable CUDA device", who);
+  constexpr int kReserve = 2048;  // per CTA: the system's share and the static shared memory
+  int stages = 0;
+  for (; occ >= 1; --occ) {
+    stages = (smem_sm / occ - kReserve) / stage_bytes;
+    if (stages >= 2) break;
+  }
+  if (occ < 1) return fail(PVL_ERR_UNSUPPORTED, "%s: D = %d does not fit in shared memory", who, p.D);
+  p.stages = stages < kMaxStages ? stages : kMaxStages;
+  const int smem = p.stages * stage_bytes;
+  st = check_cuda(cudaFuncSetAttribute(adaln_kernel<kV, kBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem), who);
+  if (st != PVL_OK) return st;
+  const long long cap = static_cast<long long>(occ) * sms;
   const long long grid = p.items < cap ? p.items : cap;
-  adaln_kernel<kV, kBwd, kStages><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
+  adaln_kernel<kV, kBwd><<<static_cast<unsigned>(grid), threads, smem, s>>>(p);
   return check_cuda(cudaGetLastError(), who);
 }
 
+// Four feature groups per thread (a few warps per row: the per-row barrier
+// and reduction are paid by fewer warps, and more CTAs share an SM); fewer
+// only where that would leave less than one warp per row.
 template <bool kBwd>
 pvl_status dispatch(const AdalnParams& p, cudaStream_t s, const char* who) {
-  const int vec_per_thread = (p.D / 8 + kThreads - 1) / kThreads;
-  if (vec_per_thread <= 1) return launch_rows<1, kBwd>(p, s, who);
-  if (vec_per_thread <= 2) return launch_rows<2, kBwd>(p, s, who);
-  if (vec_per_thread <= 3) return launch_rows<3, kBwd>(p, s, who);
-  return launch_rows<4, kBwd>(p, s, who);
+  const int nvec = p.D / 8;
+  if (nvec >= 4 * 32) return launch_rows<4, kBwd>(p, s, who);
+  if (nvec >= 2 * 32) return launch_rows<2, kBwd>(p, s, who);
+  return launch_rows<1, kBwd>(p, s, who);
 }
 
 pvl_status validate(const char* who, const void* const* ptrs, int nptrs, int B, int N, int D, float eps) {
@@ -376,7 +500,8 @@ pvl_status validate(const char* who, const void* const* ptrs, int nptrs, int B, 
   if (!(eps >= 0.0f) || !(eps < 1e30f)) return fail(PVL_ERR_INVALID_ARG, "%s: eps must be >= 0 and finite", who);
   if (D % 8 != 0 || D > kMaxD)
     return fail(PVL_ERR_UNSUPPORTED, "%s: D = %d (supported: multiples of 8 up to %d)", who, D, kMaxD);
-  if (static_cast<long long>(B) * N * D >= (1ll << 40)) return fail(PVL_ERR_UNSUPPORTED, "%s: tensor too large", who);
+  if (static_cast<long long>(B) * N * D >= (1ll << 40) || N > (1 << 30))
+    return fail(PVL_ERR_UNSUPPORTED, "%s: tensor too large", who);
   for (int i = 0; i < nptrs; ++i)
     if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0)
       return fail(PVL_ERR_UNSUPPORTED, "%s: pointer argument %d is not 16-byte aligned", who, i);
@@ -410,6 +535,7 @@ extern "C" pvl_status adaln_fwd(const pvl_bf16* x, const float* shift, const flo
   p.B = B;
   p.N = N;
   p.D = D;
+  p.units = N;
   p.items = static_cast<long long>(B) * N;
   p.eps = eps;
   p.timeout_ns = kDefaultTimeoutNs;
@@ -444,12 +570,13 @@ extern "C" pvl_status adaln_bwd(const pvl_bf16* x, const float* scale, const pvl
   p.N = N;
   p.D = D;
   p.n_tiles = n_tiles_of(N);
+  p.units = p.n_tiles;
   p.items = static_cast<long long>(B) * p.n_tiles;
   p.eps = eps;
   p.timeout_ns = kDefaultTimeoutNs;
   st = dispatch<true>(p, s, "adaln_bwd launch");
   if (st != PVL_OK) return st;
-  const long long n = 2ll * B * D;
-  adaln_bwd_finalize<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(p.part, B, D, p.n_tiles, dshift, dscale);
+  const dim3 fin_grid(2 * B, (D + 127) / 128);
+  adaln_bwd_finalize<<<fin_grid, kFinThreads, 0, s>>>(p.part, B, D, p.n_tiles, dshift, dscale);
   return check_cuda(cudaGetLastError(), "adaln_bwd finalize launch");
 }
