@@ -278,8 +278,10 @@ PVL_API pvl_status masked_attn_bwd_no_alloc(const pvl_bf16* q, const pvl_bf16* k
  * D a multiple of 8, at most 8192; eps >= 0 (1e-6 is the usual choice).
  * mean, rstd: optional (null allowed) dev fp32 [B, N] row statistics the
  * forward can write; the backward recomputes them from x and needs neither.
- * adaln_bwd ws: dev scratch of adaln_bwd_ws_bytes(B, N, D) bytes (per-tile
- * partial sums of dshift / dscale); contents on entry are ignored.
+ * adaln_bwd ws: dev scratch of adaln_bwd_ws_bytes(B, N, D) bytes (partial
+ * sums of dshift / dscale, one per (CTA, batch row): 2 * (min(B N, 2048) +
+ * B - 1) * D fp32); contents on entry are ignored.  The partials are added
+ * in a fixed order: repeated calls on one GPU give the same bits.
  * All pointers 16-byte aligned (mean / rstd 4-byte).  Errors: INVALID_ARG
  * for null pointers, sizes < 1, a negative eps or a short workspace;
  * UNSUPPORTED for other D or misaligned pointers; CUDA for launch failures;

@@ -23,12 +23,13 @@
 //     reduction (two-level, as the page describes), and the statistics never
 //     leave the chip; the modulation is applied on the way out.  The barrier
 //     that opens a row also frees the previous row's stage;
-//   - backward, the rows of a work item (one batch row, a tile of
-//     kRowsPerTile tokens) accumulate dshift / dscale in the registers of
-//     the threads that own each feature: the sequence-direction reduction of
-//     the page's D-tile scheme, with coalesced reads along the features.
-//     Each item writes its partial sums once; a small kernel adds the tiles'
-//     partials per batch row, in a fixed order (deterministic).
+//   - the rows are split evenly among the CTAs in contiguous ranges;
+//     backward, each CTA accumulates dshift / dscale over its rows of one
+//     batch row in the registers of the threads that own each feature (the
+//     sequence-direction reduction of the page's D-tile scheme, with
+//     coalesced reads along the features) and writes one partial sum per
+//     batch row it meets; a small kernel adds the partials per batch row in
+//     a fixed order (deterministic).
 // Every wait is bounded; on expiry the CTA records the failure, waits for
 // its copies in flight and returns.
 #include <cuda_runtime.h>
@@ -41,7 +42,7 @@ namespace {
 constexpr int kMaxThreads = 512;
 constexpr int kMaxWarps = kMaxThreads / 32;
 constexpr int kMaxStages = 8;
-constexpr int kRowsPerTile = 64;  // backward work item: tokens of one batch row
+constexpr int kMaxCtas = 2048;    // CTAs per launch at most (bounds the partial-sum slots)
 constexpr int kMaxD = 8192;
 
 enum AdalnSite : uint32_t { kSiteRowFull = 41 };
@@ -118,11 +119,12 @@ struct AdalnParams {
   __nv_bfloat16* out;       // y forward, dx backward
   float* mean;              // forward, optional
   float* rstd;              // forward, optional
-  float* part;              // backward: [2][B * n_tiles][D] tile partials
+  float* part;              // backward: [2][n_slots][D] partial sums
   DeviceError* err;
-  int B, N, D, n_tiles;
-  int units;                // rows per batch row: N forward, n_tiles backward
-  long long items;          // forward: rows; backward: B * n_tiles
+  int B, N, D;
+  long long rows;           // B * N
+  long long rows_per_cta;   // CTA c takes rows [c R, (c + 1) R) of the B * N
+  int n_slots;              // partial-sum slots: kMaxCtas (at most B * N) + B - 1
   int stages;               // shared-memory row stages, 2..kMaxStages
   float eps;
   uint64_t timeout_ns;
@@ -142,9 +144,12 @@ constexpr int max_regs() {
   return kBwd ? (kV == 1 ? 64 : (kV == 2 ? 96 : 128)) : (kV == 1 ? 48 : (kV == 2 ? 64 : (kV == 3 ? 96 : 128)));
 }
 
-// One CTA walks its items (forward: rows blockIdx.x, blockIdx.x + gridDim.x,
-// ...; backward: tiles of kRowsPerTile tokens of one batch row) with every
-// thread owning feature groups t, t + blockDim.x, ... (kV of them at most).
+// CTA c takes the rows [c R, (c + 1) R) of the B * N (the last CTA fewer):
+// every CTA gets the same number of rows to within one.  Its rows split into
+// segments at batch-row boundaries; every thread owns the feature groups
+// t, t + blockDim.x, ... (kV of them at most) of every row.  Backward, a
+// segment's dshift / dscale sums go to partial-sum slot c + b (b its batch
+// row; no two (CTA, batch row) pairs that meet share a slot).
 template <int kV, bool kBwd>
 __global__ void __maxnreg__((max_regs<kV, kBwd>())) adaln_kernel(const AdalnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -162,6 +167,8 @@ __global__ void __maxnreg__((max_regs<kV, kBwd>())) adaln_kernel(const AdalnPara
   const int S = p.stages;
   const float inv_d = 1.0f / static_cast<float>(D);
   const KernelCtl ctl{p.err, &abort_s, p.timeout_ns};
+  const long long r_begin = static_cast<long long>(blockIdx.x) * p.rows_per_cta;
+  const long long r_end = min(r_begin + p.rows_per_cta, p.rows);
 
   if (t == 0) {
     abort_s = 0;
@@ -170,37 +177,20 @@ __global__ void __maxnreg__((max_regs<kV, kBwd>())) adaln_kernel(const AdalnPara
   }
   __syncthreads();
 
-  // Item -> (batch row, unit): advanced incrementally, no divisions per row.
-  auto advance = [&](int& b, int& u) {
-    u += gridDim.x;
-    if (u >= p.units) {
-      b += u / p.units;
-      u %= p.units;
-    }
-  };
-  auto rows_of = [&](int u) -> int { return kBwd ? min(kRowsPerTile, p.N - u * kRowsPerTile) : 1; };
-  auto row0_of = [&](int b, int u) -> long long {
-    return static_cast<long long>(b) * p.N + (kBwd ? u * kRowsPerTile : u);
-  };
-
-  // Producer state (thread 0): the next row to load.
-  const int first_b = static_cast<int>(blockIdx.x / p.units), first_u = static_cast<int>(blockIdx.x % p.units);
-  int ld_b = first_b, ld_u = first_u, ld_k = 0;
+  // Producer (thread 0): the CTA's rows in order, x and dy of a row into one
+  // stage.
+  long long ld_r = r_begin;
   uint32_t ld_n = 0;  // rows issued
   int ld_st = 0;
   auto issue_next = [&]() {
-    if (ld_b >= p.B) return;
-    const long long r = row0_of(ld_b, ld_u) + ld_k;
+    if (ld_r >= r_end) return;
     uint8_t* dst = smem + static_cast<size_t>(ld_st) * kTensors * RB;
     mbar_arrive_expect_tx(&full[ld_st], kTensors * D * 2);
-    bulk_load(dst, p.x + r * D, D * 2, &full[ld_st]);
-    if (kBwd) bulk_load(dst + RB, p.dy + r * D, D * 2, &full[ld_st]);
+    bulk_load(dst, p.x + ld_r * D, D * 2, &full[ld_st]);
+    if (kBwd) bulk_load(dst + RB, p.dy + ld_r * D, D * 2, &full[ld_st]);
+    ++ld_r;
     ++ld_n;
     if (++ld_st == S) ld_st = 0;
-    if (++ld_k == rows_of(ld_u)) {
-      ld_k = 0;
-      advance(ld_b, ld_u);
-    }
   };
   if (t == 0)
     for (int s = 0; s < S; ++s) issue_next();
@@ -209,25 +199,20 @@ __global__ void __maxnreg__((max_regs<kV, kBwd>())) adaln_kernel(const AdalnPara
   int use_st = 0;
   uint32_t use_ph = 0;
   bool alive = true;
-  // per-thread modulation of the owned feature groups (forward), reloaded
-  // when the batch row changes
+  // per-thread modulation of the owned feature groups (forward), loaded per
+  // segment
   float2 mod[kBwd ? 1 : kV][4];  // 1 + scale
   float2 sh[kBwd ? 1 : kV][4];   // shift
-  int cur_b = -1;
-  int it_b = first_b, it_u = first_u;
-  for (; it_b < p.B && alive; advance(it_b, it_u)) {
-    const int b = it_b;
-    const int nrows = rows_of(it_u);
-    const long long row0 = row0_of(b, it_u);
+  int b = r_begin < r_end ? static_cast<int>(r_begin / p.N) : p.B;
+  for (long long r = r_begin; r < r_end && alive; ++b) {
+    const long long seg_end = min(r_end, static_cast<long long>(b + 1) * p.N);
     float2 acc_s[kBwd ? kV : 1][4], acc_c[kBwd ? kV : 1][4];  // dshift, dscale partials
-    const bool reload = !kBwd && b != cur_b;
-    cur_b = b;
 #pragma unroll
     for (int i = 0; i < kV; ++i) {
       if (kBwd) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc_s[i][e] = acc_c[i][e] = make_float2(0.f, 0.f);
-      } else if (reload) {
+      } else {
         const int v = t + i * nthr;
         if (v < nvec) {
           float2 sc[4], sf[4];
@@ -242,7 +227,7 @@ __global__ void __maxnreg__((max_regs<kV, kBwd>())) adaln_kernel(const AdalnPara
       }
     }
     const float* scale_row = p.scale + static_cast<size_t>(b) * D;
-    for (int k = 0; k < nrows; ++k) {
+    for (; r < seg_end; ++r) {
       if (!__syncthreads_and(mbar_wait(&full[use_st], use_ph, ctl, kSiteRowFull))) {
         alive = false;
         break;
@@ -251,7 +236,6 @@ __global__ void __maxnreg__((max_regs<kV, kBwd>())) adaln_kernel(const AdalnPara
       // table are free, so the stage is refilled now.
       if (t == 0 && use_n > 0) issue_next();
       const uint8_t* src = smem + static_cast<size_t>(use_st) * kTensors * RB;
-      const long long r = row0 + k;
       // Row statistics from shifted sums: with K the row's first element and
       // d = x - K, S1 = sum d, S2 = sum d^2, m1 = S1/D, mean = K + m1,
       // var = S2/D - m1^2 and xh = (d - m1) r.  K is a sample of the row, so
@@ -365,10 +349,10 @@ __global__ void __maxnreg__((max_regs<kV, kBwd>())) adaln_kernel(const AdalnPara
     }
     if (!alive) break;
     if (kBwd) {
-      // this item's partial modulation gradients, coalesced along the features
-      const long long item = static_cast<long long>(b) * p.units + it_u;
-      float* ps = p.part + static_cast<size_t>(item) * D;
-      float* pc = p.part + (static_cast<size_t>(p.items) + item) * D;
+      // the segment's partial modulation gradients, coalesced along the features
+      const size_t slot = static_cast<size_t>(blockIdx.x) + b;
+      float* ps = p.part + slot * D;
+      float* pc = p.part + (static_cast<size_t>(p.n_slots) + slot) * D;
 #pragma unroll
       for (int i = 0; i < kV; ++i) {
         const int v = t + i * nthr;
@@ -389,30 +373,34 @@ __global__ void __maxnreg__((max_regs<kV, kBwd>())) adaln_kernel(const AdalnPara
   __syncthreads();
 }
 
-// dshift[b, d] / dscale[b, d] = sum over the batch row's tiles.  A CTA
-// (blockIdx.x: batch row, then dshift / dscale; blockIdx.y: feature block)
-// covers 128 features of one (batch row, output): lane l of warp w adds the
-// float4 at features 4l.. of tiles w, w + 8, w + 16, ... (four loads in
+// dshift[b, d] / dscale[b, d] = sum of the slots c + b of the CTAs c that
+// met batch row b, in CTA order.  A CTA (blockIdx.x: batch row, then dshift
+// / dscale; blockIdx.y: 128-feature block) has lane l of warp w add the
+// float4 at features 4l.. of CTAs c0 + w, c0 + w + 8, ... (four loads in
 // flight), then warp 0 adds the eight warps' sums in warp order.  The order
 // of every addition is fixed: the result is deterministic.
 constexpr int kFinThreads = 256;
-__global__ void __launch_bounds__(kFinThreads) adaln_bwd_finalize(const float* __restrict__ part, int B, int D,
-                                                                  int n_tiles, float* __restrict__ dshift,
+__global__ void __launch_bounds__(kFinThreads) adaln_bwd_finalize(const float* __restrict__ part, int B, int N, int D,
+                                                                  long long rows_per_cta, int n_slots,
+                                                                  float* __restrict__ dshift,
                                                                   float* __restrict__ dscale) {
   __shared__ float4 acc[kFinThreads / 32][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int d = blockIdx.y * 128 + lane * 4;
   const int b = static_cast<int>(blockIdx.x % B);
   const bool is_scale = static_cast<int>(blockIdx.x) >= B;
-  const float* src = part + (is_scale ? static_cast<size_t>(B) * n_tiles * D : 0) + static_cast<size_t>(b) * n_tiles * D + d;
+  const int c0 = static_cast<int>(static_cast<long long>(b) * N / rows_per_cta);
+  const int c1 = static_cast<int>((static_cast<long long>(b + 1) * N - 1) / rows_per_cta);  // inclusive
+  const int n = c1 - c0 + 1;
+  const float* src = part + (is_scale ? static_cast<size_t>(n_slots) * D : 0) + (static_cast<size_t>(c0) + b) * D + d;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   if (d < D) {
     constexpr int kW = kFinThreads / 32;
-    int tl = w;
-    for (; tl + 3 * kW < n_tiles; tl += 4 * kW) {
+    int i = w;
+    for (; i + 3 * kW < n; i += 4 * kW) {
       float4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(tl + u * kW) * D));
+      for (int u = 0; u < 4; ++u) v[u] = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(i + u * kW) * D));
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         s.x += v[u].x;
@@ -421,8 +409,8 @@ __global__ void __launch_bounds__(kFinThreads) adaln_bwd_finalize(const float* _
         s.w += v[u].w;
       }
     }
-    for (; tl < n_tiles; tl += kW) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(tl) * D));
+    for (; i < n; i += kW) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(i) * D));
       s.x += v.x;
       s.y += v.y;
       s.z += v.z;
@@ -451,7 +439,7 @@ __global__ void __launch_bounds__(kFinThreads) adaln_bwd_finalize(const float* _
 // as registers allow; the shared memory of the SM split among them as row
 // stages (2 to kMaxStages).
 template <int kV, bool kBwd>
-pvl_status launch_rows(AdalnParams p, cudaStream_t s, const char* who) {
+pvl_status launch_rows(AdalnParams p, cudaStream_t s, const char* who, long long* rows_per_cta) {
   const int nvec = p.D / 8;
   const int threads = ((nvec + kV - 1) / kV + 31) / 32 * 32;
   const int stage_bytes = (kBwd ? 2 : 1) * row_bytes(p.D);
@@ -476,8 +464,12 @@ pvl_status launch_rows(AdalnParams p, cudaStream_t s, const char* who) {
   const int smem = p.stages * stage_bytes;
   st = check_cuda(cudaFuncSetAttribute(adaln_kernel<kV, kBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem), who);
   if (st != PVL_OK) return st;
-  const long long cap = static_cast<long long>(occ) * sms;
-  const long long grid = p.items < cap ? p.items : cap;
+  long long grid = static_cast<long long>(occ) * sms;
+  if (grid > kMaxCtas) grid = kMaxCtas;
+  if (grid > p.rows) grid = p.rows;
+  p.rows_per_cta = (p.rows + grid - 1) / grid;
+  grid = (p.rows + p.rows_per_cta - 1) / p.rows_per_cta;
+  *rows_per_cta = p.rows_per_cta;
   adaln_kernel<kV, kBwd><<<static_cast<unsigned>(grid), threads, smem, s>>>(p);
   return check_cuda(cudaGetLastError(), who);
 }
@@ -486,11 +478,11 @@ pvl_status launch_rows(AdalnParams p, cudaStream_t s, const char* who) {
 // and reduction are paid by fewer warps, and more CTAs share an SM); fewer
 // only where that would leave less than one warp per row.
 template <bool kBwd>
-pvl_status dispatch(const AdalnParams& p, cudaStream_t s, const char* who) {
+pvl_status dispatch(const AdalnParams& p, cudaStream_t s, const char* who, long long* rows_per_cta) {
   const int nvec = p.D / 8;
-  if (nvec >= 4 * 32) return launch_rows<4, kBwd>(p, s, who);
-  if (nvec >= 2 * 32) return launch_rows<2, kBwd>(p, s, who);
-  return launch_rows<1, kBwd>(p, s, who);
+  if (nvec >= 4 * 32) return launch_rows<4, kBwd>(p, s, who, rows_per_cta);
+  if (nvec >= 2 * 32) return launch_rows<2, kBwd>(p, s, who, rows_per_cta);
+  return launch_rows<1, kBwd>(p, s, who, rows_per_cta);
 }
 
 pvl_status validate(const char* who, const void* const* ptrs, int nptrs, int B, int N, int D, float eps) {
@@ -500,7 +492,7 @@ pvl_status validate(const char* who, const void* const* ptrs, int nptrs, int B, 
   if (!(eps >= 0.0f) || !(eps < 1e30f)) return fail(PVL_ERR_INVALID_ARG, "%s: eps must be >= 0 and finite", who);
   if (D % 8 != 0 || D > kMaxD)
     return fail(PVL_ERR_UNSUPPORTED, "%s: D = %d (supported: multiples of 8 up to %d)", who, D, kMaxD);
-  if (static_cast<long long>(B) * N * D >= (1ll << 40) || N > (1 << 30))
+  if (static_cast<long long>(B) * N * D >= (1ll << 40) || N > (1 << 30) || B > (1 << 30))
     return fail(PVL_ERR_UNSUPPORTED, "%s: tensor too large", who);
   for (int i = 0; i < nptrs; ++i)
     if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0)
@@ -508,7 +500,11 @@ pvl_status validate(const char* who, const void* const* ptrs, int nptrs, int B, 
   return PVL_OK;
 }
 
-int n_tiles_of(int N) { return (N + kRowsPerTile - 1) / kRowsPerTile; }
+// partial-sum slots of the backward: one per (CTA, batch row) pair that meets
+int slots_of(int B, int N) {
+  const long long rows = static_cast<long long>(B) * N;
+  return static_cast<int>((rows < kMaxCtas ? rows : kMaxCtas) + B - 1);
+}
 
 }  // namespace
 }  // namespace pvl
@@ -535,16 +531,16 @@ extern "C" pvl_status adaln_fwd(const pvl_bf16* x, const float* shift, const flo
   p.B = B;
   p.N = N;
   p.D = D;
-  p.units = N;
-  p.items = static_cast<long long>(B) * N;
+  p.rows = static_cast<long long>(B) * N;
   p.eps = eps;
   p.timeout_ns = kDefaultTimeoutNs;
-  return dispatch<false>(p, reinterpret_cast<cudaStream_t>(stream), "adaln_fwd launch");
+  long long rows_per_cta = 0;
+  return dispatch<false>(p, reinterpret_cast<cudaStream_t>(stream), "adaln_fwd launch", &rows_per_cta);
 }
 
 extern "C" size_t adaln_bwd_ws_bytes(int B, int N, int D) {
   if (B < 1 || N < 1 || D < 1) return 0;
-  return 2ull * B * n_tiles_of(N) * D * sizeof(float);
+  return 2ull * slots_of(B, N) * D * sizeof(float);
 }
 
 extern "C" pvl_status adaln_bwd(const pvl_bf16* x, const float* scale, const pvl_bf16* dy, int B, int N, int D,
@@ -569,14 +565,14 @@ extern "C" pvl_status adaln_bwd(const pvl_bf16* x, const float* scale, const pvl
   p.B = B;
   p.N = N;
   p.D = D;
-  p.n_tiles = n_tiles_of(N);
-  p.units = p.n_tiles;
-  p.items = static_cast<long long>(B) * p.n_tiles;
+  p.rows = static_cast<long long>(B) * N;
+  p.n_slots = slots_of(B, N);
   p.eps = eps;
   p.timeout_ns = kDefaultTimeoutNs;
-  st = dispatch<true>(p, s, "adaln_bwd launch");
+  long long rows_per_cta = 0;
+  st = dispatch<true>(p, s, "adaln_bwd launch", &rows_per_cta);
   if (st != PVL_OK) return st;
   const dim3 fin_grid(2 * B, (D + 127) / 128);
-  adaln_bwd_finalize<<<fin_grid, kFinThreads, 0, s>>>(p.part, B, D, p.n_tiles, dshift, dscale);
+  adaln_bwd_finalize<<<fin_grid, kFinThreads, 0, s>>>(p.part, B, N, D, rows_per_cta, p.n_slots, dshift, dscale);
   return check_cuda(cudaGetLastError(), "adaln_bwd finalize launch");
 }

@@ -79,7 +79,8 @@ def test_host_validation_without_gpu(lib):
     assert lib.adaln_fwd(dummy, dummy, dummy, 1, 4, 8200, 1e-6, dummy, null, null, null) == 2
     assert lib.adaln_fwd(dummy, dummy, dummy, 1, 4, 64, -1.0, dummy, null, null, null) == 1
     assert lib.adaln_bwd(dummy, dummy, dummy, 1, 4, 64, 1e-6, dummy, dummy, dummy, dummy, 0, null) == 1
-    assert lib.adaln_bwd_ws_bytes(2, 100, 64) == 2 * 2 * 2 * 64 * 4   # two 64-token tiles per row
+    assert lib.adaln_bwd_ws_bytes(2, 100, 64) == 2 * (200 + 1) * 64 * 4      # a slot per (CTA, batch row)
+    assert lib.adaln_bwd_ws_bytes(1, 64000, 5120) == 2 * 2048 * 5120 * 4     # at most 2048 CTAs
 
 
 def test_tile_map_layout_host(lib):

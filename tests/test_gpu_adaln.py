@@ -68,7 +68,9 @@ def run(pvl, x, shift, scale, dy, eps):
 
 
 @pytest.mark.parametrize("B,N,D", [(2, 7, 8), (3, 130, 64), (2, 257, 1536), (1, 300, 3072), (2, 129, 5120),
-                                   (1, 65, 8192), (1, 1, 2048), (2, 64, 5128)])
+                                   (1, 65, 8192), (1, 1, 2048), (2, 64, 5128),
+                                   # more rows than CTAs: row ranges that cross batch rows
+                                   (3000, 3, 1024), (5, 4001, 512), (2, 70000, 64), (3, 9001, 5120)])
 def test_against_oracle(pvl, B, N, D):
     x, shift, scale, dy = inputs(B, N, D, seed=B * 1000 + N + D)
     eps = 1e-6
