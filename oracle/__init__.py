@@ -19,6 +19,10 @@ What it computes, written from the LingBot-VA packing reports:
   in which query i attends key j iff seq_id[i] == seq_id[j] >= 0, and its
   analytic gradient ("furniture_packing_variable_length", the seq_id = -1
   masking paragraph; "lingbot_va_attn_profiling", doc_id[q] == doc_id[k]).
+- ``loss.masked_mse`` / ``loss.masked_mse_grad``: the squared-error loss
+  averaged over valid frames only (frame_valid = f < valid_frames[b]), and
+  its gradient ("lingbot_va_packing" §2.1, compute_loss;
+  "furniture_packing_variable_length", the loss paragraph).
 - ``adaln.adaln_fwd`` / ``adaln.adaln_bwd``: layer norm over the feature
   dimension followed by the AdaLN modulation y = xh (1 + scale) + shift, and
   its gradient with the modulation gradients summed over the sequence
@@ -31,5 +35,6 @@ scaled_dot_product_attention) and the pages' packed == separate invariant.
 
 from .adaln import adaln_bwd, adaln_fwd  # noqa: F401
 from .attention import attention_bwd, attention_fwd, effective_pairs  # noqa: F401
+from .loss import frame_valid_tokens, masked_mse, masked_mse_grad, valid_from_seq_id  # noqa: F401
 from .seq_ids import build_seq_ids  # noqa: F401
 from .tile_map import EMPTY, FULL, PARTIAL, build_tile_map, tile_stats  # noqa: F401
