@@ -12,6 +12,10 @@ backward 10 D flops per pair and head).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
+`--workload adaln64k` measures the fused LayerNorm-Modulate forward and
+backward, `--workload loss64k` the frame_valid-masked loss with its gradient
+(both HBM bound, in GB/s).
+
 `--workload cross_concat64k` (or cross_padded) measures cross attention
 instead: the same episodes as queries at 38 tokens per frame and as keys at 16
 tokens per frame, each side with its own seq_ids (12 launches per step: one
@@ -502,6 +506,138 @@ def run_adaln(args):
         dist.destroy_process_group()
 
 
+LOSS_GRID = 128     # latent positions per frame (8 x 16)
+LOSS_C = 48         # latent channels
+
+
+def run_loss(args):
+    """The frame_valid-masked squared-error loss with its gradient in the same
+    pass ("lingbot_va_packing" §2.1, compute_loss) on the 64k pack's episodes
+    at the latent's own grid: 8 x 16 positions and 48 channels per frame
+    (the latent shape (48, F, 8, 16) of the attention profiling report), over
+    the pack's frame capacity (65,536 // 38 frames).  HBM bound: the metric is
+    algorithmic bytes per second (pred and target read on valid positions,
+    the gradient written everywhere, the ids read once).  The tensors are
+    about 21 MB each, inside L2, so L2 is flushed before every timed call."""
+    import torch
+    import packed_variable_length_gb300 as pvl
+    import workloads as wl
+
+    rank, world, local = dist_setup(args.gpus)
+    lay = wl.config_layout(4)
+    frames = lay.L // lay.tokens_per_frame
+    B, L, C = lay.B, frames * LOSS_GRID, LOSS_C
+    host = wl.make_loss_tensors(B, L, C, 2606)
+    dev = {k: v.cuda() for k, v in host.items()}
+    sid = pvl.pack_build_seq_ids(lay.seg_frames, lay.seg_valid, LOSS_GRID, L)
+    n_valid = int((sid >= 0).sum().item())
+    grad = torch.empty_like(dev["pred"])
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(pvl.masked_mse_ws_bytes(B, L, C), dtype=torch.uint8, device="cuda")
+    flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")    # 256 MB > L2
+    sink = torch.empty(1, dtype=torch.float32, device="cuda")
+    bytes_step = 4 * n_valid * C + 2 * B * L * C + 4 * B * L + 4
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step():
+        pvl.masked_mse_loss(dev["pred"], dev["target"], sid, grad=grad, loss=loss, ws=ws)
+
+    # L2 is flushed by reading the buffer (clean lines): a written flush would
+    # leave 129 MB of dirty lines whose write-back lands inside the next call
+    for _ in range(args.warmup):
+        torch.sum(flush, dim=0, out=sink)
+        step()
+    torch.cuda.synchronize()
+    pvl.device_error()
+    pairs = [(ev(), ev()) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    for a, b in pairs:
+        torch.sum(flush, dim=0, out=sink)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    pvl.device_error()
+    ms_step = max_over_ranks(sum(a.elapsed_time(b) for a, b in pairs), world) / args.steps
+    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+
+    pin = {k: v.pin_memory() for k, v in host.items()}
+    loss_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
+
+    def e2e_step():
+        for k in host:
+            dev[k].copy_(pin[k], non_blocking=True)
+        s = pvl.pack_build_seq_ids(lay.seg_frames, lay.seg_valid, LOSS_GRID, L, out=sid)
+        pvl.masked_mse_loss(dev["pred"], dev["target"], s, grad=grad, loss=loss, ws=ws)
+        loss_host.copy_(loss, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    pvl.device_error()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    peaks = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    result = {
+        "metric": "frame_valid-masked loss + gradient algorithmic GB/s at 1 GB300",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in/out, fp32 arithmetic, fp64 cross-CTA sum", "data": "synthetic",
+        "config": {"workload": (f"loss64k: the 64k pack's {lay.K} episodes (latent F = {lay.seg_frames[0].tolist()}) "
+                                f"on the latent grid, {LOSS_GRID} positions x {C} channels per frame, "
+                                f"{frames} frames of capacity (L = {L}, {n_valid} valid positions)"),
+                   "B": B, "L": L, "C": C, "valid_positions": n_valid,
+                   "l2": "pred, target, grad are 21 MB each (inside L2): a 256 MB buffer is read before every "
+                         "timed call, outside its events (a read leaves clean lines, so no write-back lands in the call)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "clocks": clk,
+        "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in pin.values()),
+                "d2h_bytes_per_step": 4,
+                "note": "per step: pred and target copied in, seq_ids built from the host segment table, the "
+                        "loss call, the loss read back"},
+        "gpu_launches": 2 * args.steps,
+        "roofline": {"kernel": "masked_mse_loss (count + loss kernels, timed together)", "bound": "hbm",
+                     "achieved": round(bytes_step / (ms_step * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(bytes_step / (ms_step * 1e-3) / 1e9 / hbm, 4), "traffic": None,
+                     "peak_note": f"of {peaks['source']} (STREAM-style copy)",
+                     "algorithmic": "4 C per valid position + 2 C per position + 4 per id, bytes per launch pair"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        valid = oracle.valid_from_seq_id(oracle.build_seq_ids(lay.seg_frames, lay.seg_valid, LOSS_GRID, L))
+        t = time.perf_counter()
+        reps = 0
+        while reps < 3 or time.perf_counter() - t < 5.0:
+            oracle.masked_mse(host["pred"], host["target"], valid)
+            oracle.masked_mse_grad(host["pred"], host["target"], valid)
+            reps += 1
+        dt = (time.perf_counter() - t) / reps
+        result["cpu_baseline"] = {"value": round(bytes_step / dt / 1e9, 3), "unit": "GB/s",
+                                  "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                                  "sample": f"fp64 numpy oracle, loss and gradient of the whole workload, "
+                                            f"{reps} repetitions, {dt:.2f} s each"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ----------------------------------------------------------- reference arm
 def run_reference(args):
     """The fp64 oracle on the host cores, one bounded sample per step: fwd + bwd
@@ -552,7 +688,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="concat64k", choices=sorted(WORKLOADS) + ["adaln64k"],
+    ap.add_argument("--workload", default="concat64k", choices=sorted(WORKLOADS) + ["adaln64k", "loss64k"],
                     help="concat64k is the headline workload; the others are smaller cases for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -562,6 +698,8 @@ def main():
         run_reference(args)
     elif args.workload == "adaln64k":
         run_adaln(args)
+    elif args.workload == "loss64k":
+        run_loss(args)
     else:
         run_gpu(args)
 

@@ -297,6 +297,43 @@ PVL_API pvl_status adaln_bwd(const pvl_bf16* x, const float* scale, const pvl_bf
                              pvl_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * masked_mse_loss / masked_mse_loss_bwd — the squared-error loss averaged
+ * over valid frames only, and its gradient ("lingbot_va_packing" §2.1,
+ * compute_loss: frame_valid = f < valid_frames[b], latent and action
+ * losses averaged over the valid frames; "furniture_packing_variable_length",
+ * the loss paragraph).  Per stream (latent or action tokens):
+ *   valid token  = seq_id >= 0 (the attention's mask; on pad-collated rows
+ *                  it is frame_valid spread over the frame's tokens)
+ *   loss         = sum_{valid} sum_c (pred - target)^2 / (C n_valid)
+ *   grad         = dloss 2 (pred - target) / (C n_valid) on valid tokens,
+ *                  0 on the others; loss = 0 and grad = 0 if n_valid = 0.
+ *
+ * pred, target, grad: dev bf16 [B, L, C] (token-major, C fastest); seq_id:
+ * dev int32 [B, L]; loss: dev fp32 [1].  C a multiple of 8; B * L < 2^31.
+ * masked_mse_loss writes the loss and, when grad is not null, the gradient
+ * scaled by the host value grad_scale in the same pass (the fused form for
+ * a loss that is the objective: grad_scale = its weight).
+ * masked_mse_loss_bwd writes only the gradient, scaled by the device value
+ * dloss[0] (the autograd form).  Padding tokens' pred and target are never
+ * read.  ws: dev scratch of masked_mse_ws_bytes(B, L, C) bytes, contents on
+ * entry ignored, one per call in flight.  The loss is deterministic for a
+ * given GPU model (fixed grid, fixed summation order).  pred, target,
+ * seq_id, grad, ws 16-byte aligned; loss, dloss 4-byte.  Errors:
+ * INVALID_ARG for null pointers, sizes < 1, a non-finite grad_scale or a
+ * short workspace; UNSUPPORTED for other C, sizes or alignment; CUDA for
+ * launch failures.
+ * ---------------------------------------------------------------------- */
+PVL_API size_t masked_mse_ws_bytes(int B, int L, int C);
+
+PVL_API pvl_status masked_mse_loss(const pvl_bf16* pred, const pvl_bf16* target, const int32_t* seq_id, int B, int L,
+                                   int C, float* loss, pvl_bf16* grad, float grad_scale, void* ws, size_t ws_bytes,
+                                   pvl_stream_t stream);
+
+PVL_API pvl_status masked_mse_loss_bwd(const pvl_bf16* pred, const pvl_bf16* target, const int32_t* seq_id, int B,
+                                       int L, int C, const float* dloss, pvl_bf16* grad, void* ws, size_t ws_bytes,
+                                       pvl_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Device error record.  Synchronises `stream`, reads and clears the current
  * device's error record.  Returns PVL_OK, PVL_ERR_TIMEOUT (a bounded wait ran
  * out; the kernel released its resources and returned), PVL_ERR_INVALID_ARG

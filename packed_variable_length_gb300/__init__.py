@@ -21,9 +21,12 @@ from .api import (  # noqa: F401
     masked_attn_bwd_no_alloc,
     masked_attn_bwd_ws_bytes,
     masked_attn_fwd,
+    masked_mse_loss,
+    masked_mse_loss_bwd,
+    masked_mse_ws_bytes,
     pack_build_seq_ids,
     tile_map_build,
     tile_map_ws_bytes,
     version,
 )
-from .autograd import adaln_modulate, packed_attention  # noqa: F401
+from .autograd import adaln_modulate, frame_valid_mse, packed_attention  # noqa: F401

@@ -39,6 +39,9 @@ SIGNATURES = {
     "adaln_fwd": (_c_int, [_p, _p, _p, _c_int, _c_int, _c_int, _c_float, _p, _p, _p, _p]),
     "adaln_bwd_ws_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "adaln_bwd": (_c_int, [_p, _p, _p, _c_int, _c_int, _c_int, _c_float, _p, _p, _p, _p, _c_size, _p]),
+    "masked_mse_ws_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "masked_mse_loss": (_c_int, [_p, _p, _p, _c_int, _c_int, _c_int, _p, _p, _c_float, _p, _c_size, _p]),
+    "masked_mse_loss_bwd": (_c_int, [_p, _p, _p, _c_int, _c_int, _c_int, _p, _p, _p, _c_size, _p]),
     "pvl_device_error": (_c_int, [_p]),
     "pvl_device_error_detail": (_c_int, [_p, _p]),
     "pvl_last_error_message": (ctypes.c_char_p, []),

@@ -346,6 +346,65 @@ def adaln_bwd(x, scale, dy, eps: float = 1e-6, dx=None, dshift=None, dscale=None
     return dx, dshift, dscale
 
 
+# ------------------------------------------------------------ masked loss
+def masked_mse_ws_bytes(B: int, L: int, C: int) -> int:
+    return int(_lib.load().masked_mse_ws_bytes(B, L, C))
+
+
+def _loss_args(pred, target, seq_id):
+    if pred.dim() != 3:
+        raise ValueError("pred must be [B, L, C]")
+    B, L, C = pred.shape
+    _need_cuda(pred, "pred", torch.bfloat16, (B, L, C))
+    _need_cuda(target, "target", torch.bfloat16, (B, L, C))
+    _need_cuda(seq_id, "seq_id", torch.int32, (B, L))
+    return B, L, C
+
+
+def masked_mse_loss(pred, target, seq_id, grad: bool | torch.Tensor = False, grad_scale: float = 1.0,
+                    loss=None, ws=None, stream=None):
+    """Squared-error loss averaged over the valid tokens (seq_id >= 0), i.e.
+    over the valid frames ("lingbot_va_packing" §2.1, compute_loss).  pred,
+    target bf16 [B, L, C]; seq_id int32 [B, L].  Returns the fp32 loss as a
+    one-element device tensor, or (loss, grad) when grad is True or a bf16
+    [B, L, C] tensor to fill: grad = grad_scale * d loss / d pred, computed
+    in the same pass."""
+    B, L, C = _loss_args(pred, target, seq_id)
+    want_grad = grad is not False and grad is not None
+    g = None
+    if want_grad:
+        g = torch.empty_like(pred) if grad is True else grad
+        _need_cuda(g, "grad", torch.bfloat16, (B, L, C))
+    loss = torch.empty(1, dtype=torch.float32, device=pred.device) if loss is None else loss
+    _need_cuda(loss, "loss", torch.float32, (1,))
+    lib = _lib.load()
+    nbytes = int(lib.masked_mse_ws_bytes(B, L, C))
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=pred.device)
+    with torch.cuda.device(pred.device):
+        _check(lib.masked_mse_loss(pred.data_ptr(), target.data_ptr(), seq_id.data_ptr(), B, L, C, loss.data_ptr(),
+                                   _ptr(g), float(grad_scale), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return (loss, g) if want_grad else loss
+
+
+def masked_mse_loss_bwd(pred, target, seq_id, dloss, grad=None, ws=None, stream=None):
+    """d loss / d pred of masked_mse_loss times the device scalar dloss (fp32, one element)."""
+    B, L, C = _loss_args(pred, target, seq_id)
+    _need_cuda(dloss, "dloss", torch.float32)
+    if dloss.numel() != 1:
+        raise ValueError("dloss must hold one element")
+    grad = torch.empty_like(pred) if grad is None else grad
+    _need_cuda(grad, "grad", torch.bfloat16, (B, L, C))
+    lib = _lib.load()
+    nbytes = int(lib.masked_mse_ws_bytes(B, L, C))
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=pred.device)
+    with torch.cuda.device(pred.device):
+        _check(lib.masked_mse_loss_bwd(pred.data_ptr(), target.data_ptr(), seq_id.data_ptr(), B, L, C,
+                                       dloss.data_ptr(), grad.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return grad
+
+
 # ------------------------------------------------------------------- errors
 def device_error(stream=None, raise_on_error: bool = True):
     """Synchronises the stream and returns (status, [code, where, block, thread])."""

@@ -58,3 +58,26 @@ def adaln_modulate(x, shift, scale, eps: float = 1e-6):
     shift / scale [B, D], differentiable ("AdaptiveLoad" §2.B); the backward
     recomputes the row statistics from x."""
     return _AdaLNModulate.apply(x, shift, scale, eps)
+
+
+class _MaskedMSE(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, pred, target, seq_id):
+        loss = api.masked_mse_loss(pred, target, seq_id)
+        ctx.save_for_backward(pred, target, seq_id)
+        return loss.view(())
+
+    @staticmethod
+    def backward(ctx, dloss):
+        pred, target, seq_id = ctx.saved_tensors
+        grad = api.masked_mse_loss_bwd(pred, target, seq_id, dloss.reshape(1).contiguous())
+        return grad, None, None
+
+
+def frame_valid_mse(pred, target, seq_id):
+    """Squared-error loss of bf16 pred [B, L, C] against target, averaged
+    over the valid tokens (seq_id >= 0: the valid frames), differentiable in
+    pred ("lingbot_va_packing" §2.1, compute_loss).  The backward reads pred
+    and target again and scales by the incoming gradient on the device."""
+    return _MaskedMSE.apply(pred, target, seq_id)
+

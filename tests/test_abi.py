@@ -48,7 +48,7 @@ def test_only_declared_symbols_are_exported(lib):
     if out.returncode != 0:
         pytest.skip("nm unavailable")
     names = {ln.split()[-1] for ln in out.stdout.splitlines() if " T " in ln}
-    ours = {n for n in names if n.startswith(("pvl_", "pack_", "tile_map", "masked_attn", "adaln_"))}
+    ours = {n for n in names if n.startswith(("pvl_", "pack_", "tile_map", "masked_attn", "masked_mse", "adaln_"))}
     assert ours == set(declared_symbols())
 
 
@@ -81,6 +81,16 @@ def test_host_validation_without_gpu(lib):
     assert lib.adaln_bwd(dummy, dummy, dummy, 1, 4, 64, 1e-6, dummy, dummy, dummy, dummy, 0, null) == 1
     assert lib.adaln_bwd_ws_bytes(2, 100, 64) == 2 * (200 + 1) * 64 * 4      # a slot per (CTA, batch row)
     assert lib.adaln_bwd_ws_bytes(1, 64000, 5120) == 2 * 2048 * 5120 * 4     # at most 2048 CTAs
+    # masked loss: C a multiple of 8, a finite grad_scale, a full workspace
+    ws = lib.masked_mse_ws_bytes(1, 10, 8)
+    assert ws > 0 and lib.masked_mse_ws_bytes(0, 10, 8) == 0
+    assert lib.masked_mse_loss(dummy, dummy, dummy, 1, 10, 12, dummy, null, 1.0, dummy, ws, null) == 2
+    assert lib.masked_mse_loss(null, dummy, dummy, 1, 10, 8, dummy, null, 1.0, dummy, ws, null) == 1
+    assert lib.masked_mse_loss(dummy, dummy, dummy, 1, 10, 8, null, null, 1.0, dummy, ws, null) == 1
+    assert lib.masked_mse_loss(dummy, dummy, dummy, 1, 10, 8, dummy, null, float("nan"), dummy, ws, null) == 1
+    assert lib.masked_mse_loss(dummy, dummy, dummy, 1, 10, 8, dummy, null, 1.0, dummy, ws - 1, null) == 1
+    assert lib.masked_mse_loss_bwd(dummy, dummy, dummy, 1, 10, 8, null, dummy, dummy, ws, null) == 1
+    assert lib.masked_mse_loss_bwd(dummy, dummy, dummy, 0, 10, 8, dummy, dummy, dummy, ws, null) == 1
 
 
 def test_tile_map_layout_host(lib):

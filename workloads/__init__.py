@@ -26,6 +26,7 @@ from .configs import (  # noqa: F401
     cross_config_layout,
     cross_layout,
     make_cross_tensors,
+    make_loss_tensors,
     make_tensors,
     random_layout,
     round_up,

@@ -222,3 +222,15 @@ def make_cross_tensors(cl: CrossLayout, device="cpu", with_grad_out: bool = True
         x = rng.standard_normal(size=(cl.B, L, cl.H, cl.D), dtype=np.float32)
         out[nm] = torch.from_numpy(x).to(torch.bfloat16).to(device)
     return out
+
+
+def make_loss_tensors(B: int, L: int, C: int, seed: int, device="cpu"):
+    """Prediction and target of the loss as bf16 [B, L, C] tensors: standard
+    normal draws from ``seed`` (prediction first)."""
+    rng = np.random.default_rng(seed)
+    out = {}
+    for nm in ("pred", "target"):
+        x = rng.standard_normal(size=(B, L, C), dtype=np.float32)
+        out[nm] = torch.from_numpy(x).to(torch.bfloat16).to(device)
+    return out
+
