@@ -23,6 +23,10 @@ What it computes, written from the LingBot-VA packing reports:
   averaged over valid frames only (frame_valid = f < valid_frames[b]), and
   its gradient ("lingbot_va_packing" §2.1, compute_loss;
   "furniture_packing_variable_length", the loss paragraph).
+- ``adaptive_load``: the dual-constraint batch size max(1, min(floor(M_mem/S),
+  floor(M_comp/S^p))), the least-squares fit of step_time ~ a + b B S^p by
+  brute force over p, the bucket split and the balance measures (coefficient
+  of variation, synchronous data-parallel throughput) ("AdaptiveLoad" §2.A, §4).
 - ``adaln.adaln_fwd`` / ``adaln.adaln_bwd``: layer norm over the feature
   dimension followed by the AdaLN modulation y = xh (1 + scale) + shift, and
   its gradient with the modulation gradients summed over the sequence
