@@ -32,6 +32,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -638,6 +639,151 @@ def run_loss(args):
         dist.destroy_process_group()
 
 
+ADAPTIVE_M_MEM = 65536        # token budget per GPU batch (the 64k pack)
+ADAPTIVE_HIDDEN = 1536        # H * D: the AdaLN width of the timed layer step
+ADAPTIVE_RANKS = 8            # simulated synchronous data-parallel ranks
+ADAPTIVE_EPISODES = 1000      # episode pool: enough that the 33 padded shapes fill their batches
+
+
+def run_adaptive(args):
+    """AdaptiveLoad's dual-constraint bucketing ("AdaptiveLoad" §2.A, §4) on
+    the library's own kernels.  The timed unit ("layer step") for a batch of B
+    episodes padded to F_pad frames (S = 38 F_pad tokens each) is masked
+    attention forward + backward (H = 12, D = 128) plus AdaLN forward +
+    backward at width 1536 over the batch's tokens, 11 launches.
+      1. Shape benchmarking: the layer step is timed over a (B, F_pad) grid
+         and step_time ~ a + b B S^p is fitted; M_comp = the fitted load of a
+         memory-bound batch at the shortest bucket (S = 38 * 104).
+      2. 1000 episode lengths drawn like workload 5's (F ~ U{103..362}; with
+         33 padded shapes, 160 would leave most buckets short of one
+         memory-bound batch) are batched three ways:
+         equal-token (B = floor(M_mem / S)), dual-constraint (B_shape), and
+         the fixed batch of 4 of the packing report's sampler.
+      3. Every batch's layer step is timed; reported per arm: the coefficient
+         of variation of the batch step times (the page's imbalance measure)
+         and the valid tokens/s of 8 simulated synchronous data-parallel ranks
+         taking the batches round-robin (each step as long as its slowest)."""
+    import torch
+    import packed_variable_length_gb300 as pvl
+    from packed_variable_length_gb300 import adaptive_load as al
+    import workloads as wl
+
+    rank, world, local = dist_setup(args.gpus)
+    H, D, T = 12, 128, wl.TOKENS_PER_FRAME
+    C = ADAPTIVE_HIDDEN
+    n_max = ADAPTIVE_M_MEM
+    g = torch.Generator().manual_seed(2607)
+    flat = {k: (torch.randn(n_max * C, generator=g)).to(torch.bfloat16).cuda() for k in ("q", "k", "v", "do")}
+    outs = {k: torch.empty(n_max * C, dtype=torch.bfloat16, device="cuda") for k in ("o", "dq", "dk", "dv", "y", "dx")}
+    shift = torch.randn(64, C, generator=g).cuda()
+    scale = (torch.randn(64, C, generator=g) * 0.3).cuda()
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def layer_step(frames, f_pad):
+        """Returns a callable running the layer step for one pad-collated batch."""
+        B = len(frames)
+        L = T * f_pad
+        v = lambda t: t[: B * L * C].view(B, L, H, D)  # noqa: E731
+        q, k, vv, do = v(flat["q"]), v(flat["k"]), v(flat["v"]), v(flat["do"])
+        o, dq, dk, dv = v(outs["o"]), v(outs["dq"]), v(outs["dk"]), v(outs["dv"])
+        x, dy = q.view(B, L, C), do.view(B, L, C)
+        y, dx = outs["y"][: B * L * C].view(B, L, C), outs["dx"][: B * L * C].view(B, L, C)
+        sid = torch.empty((B, L), dtype=torch.int32, device="cuda")
+        tm_ws = torch.empty(pvl.tile_map_ws_bytes(B, L), dtype=torch.uint8, device="cuda")
+        lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+        bws = torch.empty(pvl.masked_attn_bwd_ws_bytes(B, L, H, D), dtype=torch.uint8, device="cuda")
+        aws = torch.empty(pvl.adaln_bwd_ws_bytes(B, L, C), dtype=torch.uint8, device="cuda")
+        dshift = torch.empty((B, C), dtype=torch.float32, device="cuda")
+        dscale = torch.empty((B, C), dtype=torch.float32, device="cuda")
+        seg_f = np.full((B, 1), f_pad, np.int32)
+        seg_v = np.asarray(frames, np.int32).reshape(B, 1)
+
+        def run():
+            pvl.pack_build_seq_ids(seg_f, seg_v, T, L, out=sid)
+            tm = pvl.tile_map_build(sid, ws=tm_ws)
+            pvl.masked_attn_fwd(q, k, vv, sid, tm, o=o, lse=lse)
+            pvl.masked_attn_bwd(q, k, vv, o, do, lse, sid, tm, dq=dq, dk=dk, dv=dv, ws=bws)
+            pvl.adaln_fwd(x, shift[:B], scale[:B], 1e-6, y=y)
+            pvl.adaln_bwd(x, scale[:B], dy, 1e-6, dx=dx, dshift=dshift, dscale=dscale, ws=aws)
+        return run
+
+    def time_step(run, reps):
+        run()
+        pairs = [(ev(), ev()) for _ in range(reps)]
+        for a, b in pairs:
+            a.record(stream)
+            run()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in pairs])) * 1e-3
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    # 1. shape benchmarking and the cost-model fit
+    shapes = [(Bn, fp) for fp in (104, 168, 232, 296, 360) for Bn in (1, 2, 4, 8, 16) if Bn * T * fp <= n_max]
+    samp = []
+    for Bn, fp in shapes:
+        samp.append((Bn, T * fp, time_step(layer_step([fp] * Bn, fp), max(3, args.steps // 10))))
+    Bs, Ss, ts = (np.array(c, dtype=np.float64) for c in zip(*samp))
+    model = al.fit_cost_model(Bs, Ss, ts)
+    s_min = T * 104
+    m_comp = al.m_comp_for(n_max, s_min, model.p)
+    # 2. three ways to batch the same 160 episodes
+    lengths = wl.bucket_sweep_lengths(1005, ADAPTIVE_EPISODES)
+    arms = {
+        "equal_token": al.DualConstraintBatchSampler(lengths, T, n_max, math.inf, model.p, seed=1005).all_batches(),
+        "dual_constraint": al.DualConstraintBatchSampler(lengths, T, n_max, m_comp, model.p, seed=1005).all_batches(),
+        "fixed_batch_4": wl.bucket_sweep_layouts(1005, ADAPTIVE_EPISODES, 4)[1],
+    }
+    # 3. every batch's layer step
+    results = {}
+    n_launch = 0
+    for name, batches in arms.items():
+        times, tokens, loads = [], [], []
+        for bt in batches:
+            frames = [int(lengths[i]) for i in bt]
+            fp = int(al.padded_frames(max(frames), 8))
+            times.append(time_step(layer_step(frames, fp), 3))
+            tokens.append(T * sum(frames))
+            loads.append(len(bt) * (T * fp) ** model.p)
+            n_launch += 11 * 4
+        tps, step_t, idle = al.simulate_data_parallel(times, tokens, ADAPTIVE_RANKS)
+        results[name] = {"batches": len(batches), "cv_step_time": round(al.coefficient_of_variation(times), 4),
+                         "cv_modelled_load": round(al.coefficient_of_variation(loads), 4),
+                         "sim_dp8_tokens_per_s": round(tps, 1), "sim_dp8_idle_fraction": round(idle, 4),
+                         "sim_dp8_cv_step": round(al.coefficient_of_variation(step_t), 4),
+                         "batch_sizes": sorted(set(len(b) for b in batches)),
+                         "total_step_time_s": round(float(sum(times)), 4)}
+    clk = clocks.stop()
+    pvl.device_error()
+    dual, base = results["dual_constraint"], results["equal_token"]
+    value = world * dual["sim_dp8_tokens_per_s"]
+    result = {
+        "metric": "valid tokens/s of 8 simulated synchronous data-parallel ranks under dual-constraint bucketing "
+                  "(layer step: masked attention fwd+bwd + AdaLN fwd+bwd, timed per batch on 1 GB300)",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": len(arms["dual_constraint"]),
+        "warmup": 1, "ms_per_step": round(1e3 * dual["total_step_time_s"] / len(arms["dual_constraint"]), 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": (f"adaptive_load: {ADAPTIVE_EPISODES} episode lengths drawn like workload 5's (F ~ U{{103..362}}, padded to "
+                                f"multiples of 8, 38 tokens/frame), M_mem = {n_max} tokens, H = {H}, D = {D}, "
+                                f"AdaLN width {C}; each batch's layer step timed (median of 3) after one warm-up"),
+                   "l2": "batches up to 65,536 tokens x 1536 (201 MB per tensor, larger than L2); no flush",
+                   "cost_model": {"a_s": model.a, "b": model.b, "p": round(model.p, 5), "r2": round(model.r2, 6),
+                                  "shapes": len(shapes)},
+                   "m_comp": m_comp, "s_ref": s_min, "arms": results,
+                   "dual_vs_equal_token_throughput": round(dual["sim_dp8_tokens_per_s"] / base["sim_dp8_tokens_per_s"], 4),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "clocks": clk,
+        "gpu_launches": n_launch,
+    }
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ----------------------------------------------------------- reference arm
 def run_reference(args):
     """The fp64 oracle on the host cores, one bounded sample per step: fwd + bwd
@@ -688,7 +834,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="concat64k", choices=sorted(WORKLOADS) + ["adaln64k", "loss64k"],
+    ap.add_argument("--workload", default="concat64k", choices=sorted(WORKLOADS) + ["adaln64k", "loss64k", "adaptive_load"],
                     help="concat64k is the headline workload; the others are smaller cases for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -700,6 +846,8 @@ def main():
         run_adaln(args)
     elif args.workload == "loss64k":
         run_loss(args)
+    elif args.workload == "adaptive_load":
+        run_adaptive(args)
     else:
         run_gpu(args)
 

@@ -29,4 +29,5 @@ from .api import (  # noqa: F401
     tile_map_ws_bytes,
     version,
 )
+from . import adaptive_load  # noqa: F401  (host-side dual-constraint bucketing)
 from .autograd import adaln_modulate, frame_valid_mse, packed_attention  # noqa: F401

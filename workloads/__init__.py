@@ -22,6 +22,7 @@ from .configs import (  # noqa: F401
     TOKENS_PER_FRAME,
     Layout,
     bucket_sweep_layouts,
+    bucket_sweep_lengths,
     config_layout,
     cross_config_layout,
     cross_layout,
