@@ -487,7 +487,8 @@ def run_adaln(args):
         "gpu_launches": 3 * args.steps,
         "roofline": {"kernel": "adaln_bwd (row kernel + tile-sum kernel, timed together)", "bound": "hbm",
                      "achieved": round(bwd_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(bwd_gbs / hbm, 4),
-                     "traffic": None, "peak_note": f"of {peaks['source']} (STREAM-style copy)",
+                     "traffic": traffic_record("adaln.cu", "adaln64k"),
+                     "peak_note": f"of {peaks['source']} (STREAM-style copy)",
                      "algorithmic": "6 N D + 12 B D bytes per launch"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
