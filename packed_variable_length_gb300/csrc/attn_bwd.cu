@@ -15,7 +15,9 @@
 //                128-row tiles), the padded query seq_ids, and a zeroed fp32
 //                dQ accumulator;
 //   bwd_main     one persistent CTA per SM over work items (b, key tile, head)
-//                in the tile map's longest-first key order.  Per item the K/V
+//                in the tile map's longest-first key order, head-major (the
+//                CTAs working at one time add into one head's dQ rows, which
+//                stay in L2).  Per item the K/V
 //                tile stays in shared memory while the non-empty query tiles
 //                stream through (FULL first, PARTIAL last), Q in a 2-stage
 //                ring, dO with the tile's LSE / Delta / seq_id rows in one:
@@ -96,7 +98,8 @@ struct BwdParams {
   int nT;   // key tiles per row (items)
   int nTq;  // query tiles per row: the length of each key tile's query list
   // Lp: Lq rounded up to whole 128-row tiles
-  long long total_items;
+  long long total_items;  // n_kt * H, head-major
+  int n_kt;               // B * nT: entries of the longest-first key-tile order
   float scale_log2;
   float scale;
   uint64_t timeout_ns;
@@ -324,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __shfl_sync(0xffffffffu, ok, 0);
     };
     for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
-      const int tile = p.k_order[w / p.H];
-      const int h = static_cast<int>(w % p.H);
+      const int tile = p.k_order[w % p.n_kt];
+      const int h = static_cast<int>(w / p.n_kt);
       const int b = tile / nT, kt = tile % nT;
       const int n = p.col_count[tile];
       if (n == 0) continue;
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, mbar_try_wait(b0, p0) & mbar_try_wait(b1, p1));
     };
     for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
-      const int tile = p.k_order[w / p.H];
+      const int tile = p.k_order[w % p.n_kt];
       const int n = p.col_count[tile];
       if (n == 0) continue;
       if (!wait1(&bar_kv_full, kv_it & 1, kSiteKvFull)) { alive = false; break; }
@@ -473,8 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
     };
     for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
-      const int tile = p.k_order[w / p.H];
-      const int h = static_cast<int>(w % p.H);
+      const int tile = p.k_order[w % p.n_kt];
+      const int h = static_cast<int>(w / p.n_kt);
       const int b = tile / nT, kt = tile % nT;
       const int n = p.col_count[tile];
       const int kpos = kt * 128 + row;
@@ -673,7 +676,8 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   prm.H = H;
   prm.nT = tm.nTk;
   prm.nTq = tm.nTq;
-  prm.total_items = static_cast<long long>(B) * tm.nTk * H;
+  prm.n_kt = B * tm.nTk;
+  prm.total_items = static_cast<long long>(prm.n_kt) * H;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.scale = scale;
   prm.timeout_ns = kDefaultTimeoutNs;

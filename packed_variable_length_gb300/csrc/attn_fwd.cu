@@ -13,8 +13,9 @@
 // Design.  One persistent CTA per SM walks work items (b, query-tile pair,
 // head): two adjacent 128-row query tiles A and B that share one stream of
 // key tiles, taken from level 1 of the tile map (256-row query tiles) in its
-// longest-first order with heads innermost (the CTAs running together read
-// the adjacent per-head slices of the same token rows), round-robin over CTAs.  Only the key tiles the map
+// longest-first order, head-major (the CTAs running together read one
+// head's K and V, 34 MB at 64k tokens, which stay in L2), round-robin over
+// CTAs.  Only the key tiles the map
 // lists as non-empty are touched, FULL ones first (no per-element mask),
 // then PARTIAL ones (mask from the seq_ids).
 //   warp 8      TMA producer: the Q pair once per item, K and V tiles into
@@ -92,7 +93,8 @@ struct FwdParams {
   float* lse;
   DeviceError* err;
   int B, Lq, Lk, H, nP, nK;  // query-tile pairs and key tiles per row
-  long long total_items;  // tiles * H, heads innermost
+  long long total_items;  // n_pairs * H, head-major
+  int n_pairs;            // B * nP: entries of the longest-first query-tile-pair order
   float scale_log2;
   uint64_t timeout_ns;
 };
@@ -278,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return __shfl_sync(0xffffffffu, ok, 0);
       };
       for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
-        const int tile = p.q_order[w / p.H];
-        const int h = static_cast<int>(w % p.H);
+        const int tile = p.q_order[w % p.n_pairs];
+        const int h = static_cast<int>(w / p.n_pairs);
         const int b = tile / nP, pp = tile % nP;
         const int n = p.row_count[tile];
         if (n == 0) continue;
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bar_v_empty[idx % kStages]);
       };
       for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
-        const int tile = p.q_order[w / p.H];
+        const int tile = p.q_order[w % p.n_pairs];
         const int n = p.row_count[tile];
         if (n == 0) continue;
         if (!wait1(&bar_q_full, q_it & 1, kSiteQFull)) { alive = false; break; }
@@ -442,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
     };
     for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
-      const int tile = p.q_order[w / p.H];
-      const int h = static_cast<int>(w % p.H);
+      const int tile = p.q_order[w % p.n_pairs];
+      const int h = static_cast<int>(w / p.n_pairs);
       const int b = tile / nP, pp = tile % nP;
       const int n = p.row_count[tile];
       const int qpos = pp * 256 + x * 128 + row;
@@ -575,7 +577,8 @@ pvl_status launch_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   prm.H = H;
   prm.nP = tm.nTq;
   prm.nK = tm.nTk;
-  prm.total_items = static_cast<long long>(B) * tm.nTq * H;
+  prm.n_pairs = B * tm.nTq;
+  prm.total_items = static_cast<long long>(prm.n_pairs) * H;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.timeout_ns = kDefaultTimeoutNs;
   const int smem = FwdSmem<D>::kBytes;
