@@ -150,13 +150,21 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest of the ranks' values (the slowest rank's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(units_per_rank: float, ms_per_step_max: float, world: int) -> float:
+    """Whole-job throughput of weak-scaled replicas: every rank processes the
+    same units per step, the job's step lasts as long as the slowest rank's."""
+    return world * units_per_rank / (ms_per_step_max * 1e-3)
 
 
 def traffic_record(kernel_file: str, workload: str):
@@ -322,7 +330,7 @@ def run_gpu(args):
 
     peaks = load_peaks()
     peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = aggregate(flops, ms_step, world) / 1e12
     bwd_achieved = flops_bwd / (bwd_ms * 1e-3) / 1e12
     traffic = traffic_record("attn_bwd.cu", args.workload)
     result = {
@@ -466,7 +474,7 @@ def run_adaln(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
     peaks = load_peaks()
     hbm = peaks["hbm_gbs"]
-    value = world * (bytes_fwd + bytes_bwd) / (ms_step * 1e-3) / 1e9
+    value = aggregate(bytes_fwd + bytes_bwd, ms_step, world) / 1e9
     bwd_gbs = bytes_bwd / (bwd_ms * 1e-3) / 1e9
     result = {
         "metric": "fused LayerNorm-Modulate fwd+bwd algorithmic GB/s and tokens/s at 1 GB300",
@@ -567,7 +575,7 @@ def run_loss(args):
     clk = clocks.stop()
     pvl.device_error()
     ms_step = max_over_ranks(sum(a.elapsed_time(b) for a, b in pairs), world) / args.steps
-    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    value = aggregate(bytes_step, ms_step, world) / 1e9
 
     pin = {k: v.pin_memory() for k, v in host.items()}
     loss_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
