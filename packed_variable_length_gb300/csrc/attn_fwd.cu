@@ -486,10 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = 2^(scale*log2e*S - m), packed bf16 over S columns [0, 64)
         const float lsum = exp_store(s_col, srow, p.scale_log2, neg_m);
         l = l * alpha + lsum;
-        // PV_x of the previous key tile has completed (S_x of this tile was
-        // issued after it); rescale O_x when the max grew.
+        // PV_x of the previous key tile has completed: S_x of this tile was
+        // issued after it by the same thread, and the commit that completed
+        // s_full tracks every earlier MMA of that thread, so its pv_done
+        // phase needs no wait of its own (only the item's last one is waited
+        // for, before the epilogue).  Rescale O_x when the max grew.
         if (j > 0) {
-          if (!waitw(&bar_pv_done[x], pv_it & 1, kSitePvDone)) { alive = false; break; }
           ++pv_it;
           const bool rescale = grow && m_ref != -INFINITY;
           if (__any_sync(0xffffffffu, rescale)) {
