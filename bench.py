@@ -128,6 +128,49 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def pipelined_e2e(n_steps, h2d, compute, d2h):
+    """Times n_steps end to end with the copies of neighbouring steps
+    overlapped: step i's inputs go in on one stream while step i-1 computes,
+    its results come back on a third while step i+1 computes.  Buffers are
+    double-buffered (b = i % 2): h2d(b) fills input set b, compute(b) reads
+    set b and writes output set b, d2h(b) reads output set b back; events
+    keep a set from being reused before its previous user is done.  Returns
+    milliseconds from the first copy in to the last copy out."""
+    import torch
+    cur = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+    in_ready = [ev(), ev()]
+    done = [ev(), ev()]       # compute of the set finished (inputs free, outputs written)
+    out_read = [ev(), ev()]   # results of the set copied back (outputs free)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(cur)
+    s_in.wait_stream(cur)
+    s_out.wait_stream(cur)
+    for i in range(n_steps):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(done[b])
+            h2d(b)
+            in_ready[b].record(s_in)
+        cur.wait_event(in_ready[b])
+        if i >= 2:
+            cur.wait_event(out_read[b])
+        compute(b)
+        done[b].record(cur)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done[b])
+            d2h(b)
+            out_read[b].record(s_out)
+    cur.wait_stream(s_out)
+    cur.wait_stream(s_in)
+    t1.record(cur)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1)
+
+
 # -------------------------------------------------------------- GPU arm
 def dist_setup(n_gpus: int):
     import torch
@@ -291,34 +334,40 @@ def run_gpu(args):
     fwd_ms = sum(t[0].elapsed_time(t[1]) for t in timers) / args.steps
     bwd_ms = sum(t[1].elapsed_time(t[2]) for t in timers) / args.steps
 
-    # end to end: pinned host buffers in, results back, copies inside the timed region
+    # end to end: every step copies its inputs in from pinned host memory and
+    # its results back, inside the timed region; neighbouring steps' copies
+    # overlap the compute (two buffer sets, three streams)
     pin = {k: v.pin_memory() for k, v in host.items()}
-    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    sets_in = [dev, {k: torch.empty_like(v) for k, v in dev.items()}]
+    sets_out = [{"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv},
+                {n: torch.empty_like(t) for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}]
+    out_host = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in so.items()} for so in sets_out]
 
-    def e2e_step():
+    def e2e_h2d(bi):
         for k in ("q", "k", "v", "do"):
-            dev[k].copy_(pin[k], non_blocking=True)
-        step()
-        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-            out_host[n].copy_(t, non_blocking=True)
+            sets_in[bi][k].copy_(pin[k], non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
+    def e2e_compute(bi):
+        di, do_ = sets_in[bi], sets_out[bi]
+        pvl.pack_build_seq_ids(lay.seg_frames, lay.seg_valid, T, L, out=sid)
+        if cross:
+            pvl.pack_build_seq_ids(lay.seg_frames, lay.seg_valid, Tk, Lk, out=ksid)
+        tm = pvl.tile_map_build(sid, ws=tm_ws, k_seq_id=ksid)
+        pvl.masked_attn_fwd(di["q"], di["k"], di["v"], sid, tm, o=do_["o"], lse=do_["lse"], k_seq_id=ksid)
+        pvl.masked_attn_bwd(di["q"], di["k"], di["v"], do_["o"], di["do"], do_["lse"], sid, tm, dq=do_["dq"],
+                            dk=do_["dk"], dv=do_["dv"], ws=bws, k_seq_id=ksid)
+
+    def e2e_d2h(bi):
+        for n, t in sets_out[bi].items():
+            out_host[bi][n].copy_(t, non_blocking=True)
+
+    e2e_steps = max(4, min(args.steps, 10))
+    pipelined_e2e(2, e2e_h2d, e2e_compute, e2e_d2h)
     barrier(world)
-    e0, e1 = ev(), ev()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, e2e_h2d, e2e_compute, e2e_d2h), world) / e2e_steps
     pvl.device_error()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
     h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("q", "k", "v", "do"))
-    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host[0].values())
 
     # tile efficiency: unmasked pairs / pairs inside the tiles the kernels
     # compute (FULL + PARTIAL), forward on 256 x 128 tiles, backward on 128 x 128
@@ -368,7 +417,9 @@ def run_gpu(args):
         "bwd_tflops": round(bwd_achieved, 2),
         "clocks": clk,
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "every step copies its Q, K, V, dO in from pinned host memory and O, LSE, dQ, dK, dV back; "
+                        "neighbouring steps' copies overlap the compute (two buffer sets, three streams)"},
         "gpu_launches": launches * args.steps,
         "roofline": {
             "kernel": "masked_attn_bwd (bwd_pre + bwd_main + bwd_convert launches, timed together)",
@@ -450,28 +501,31 @@ def run_adaln(args):
     bwd_ms = sum(t[1].elapsed_time(t[2]) for t in timers) / args.steps
 
     pin = {k: v.pin_memory() for k, v in host.items()}
-    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                for n, t in (("y", y), ("dx", dx), ("dshift", dshift), ("dscale", dscale))}
+    sets_in = [dev, {k: torch.empty_like(v) for k, v in dev.items()}]
+    sets_out = [{"y": y, "dx": dx, "dshift": dshift, "dscale": dscale},
+                {n: torch.empty_like(t) for n, t in (("y", y), ("dx", dx), ("dshift", dshift), ("dscale", dscale))}]
+    out_host = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in so.items()} for so in sets_out]
 
-    def e2e_step():
+    def e2e_h2d(bi):
         for k in host:
-            dev[k].copy_(pin[k], non_blocking=True)
-        step()
-        for n, t in (("y", y), ("dx", dx), ("dshift", dshift), ("dscale", dscale)):
-            out_host[n].copy_(t, non_blocking=True)
+            sets_in[bi][k].copy_(pin[k], non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    def e2e_compute(bi):
+        di, do_ = sets_in[bi], sets_out[bi]
+        pvl.adaln_fwd(di["x"], di["shift"], di["scale"], 1e-6, y=do_["y"])
+        pvl.adaln_bwd(di["x"], di["scale"], di["dy"], 1e-6, dx=do_["dx"], dshift=do_["dshift"],
+                      dscale=do_["dscale"], ws=ws)
+
+    def e2e_d2h(bi):
+        for n, t in sets_out[bi].items():
+            out_host[bi][n].copy_(t, non_blocking=True)
+
+    e2e_steps = max(4, min(args.steps, 10))
+    pipelined_e2e(2, e2e_h2d, e2e_compute, e2e_d2h)
+    barrier(world)
+    e2e_ms = pipelined_e2e(e2e_steps, e2e_h2d, e2e_compute, e2e_d2h)
     pvl.device_error()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, world) / e2e_steps
     peaks = load_peaks()
     hbm = peaks["hbm_gbs"]
     value = aggregate(bytes_fwd + bytes_bwd, ms_step, world) / 1e9
@@ -491,7 +545,9 @@ def run_adaln(args):
         "e2e": {"value": round(world * (bytes_fwd + bytes_bwd) / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in pin.values()),
-                "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in out_host.values())},
+                "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in out_host[0].values()),
+                "note": "every step copies x, dy, shift, scale in and y, dx, dshift, dscale back; neighbouring "
+                        "steps' copies overlap the compute (two buffer sets, three streams)"},
         "gpu_launches": 3 * args.steps,
         "roofline": {"kernel": "adaln_bwd (row kernel + tile-sum kernel, timed together)", "bound": "hbm",
                      "achieved": round(bwd_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(bwd_gbs / hbm, 4),
@@ -578,27 +634,28 @@ def run_loss(args):
     value = aggregate(bytes_step, ms_step, world) / 1e9
 
     pin = {k: v.pin_memory() for k, v in host.items()}
-    loss_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
+    sets_in = [dev, {k: torch.empty_like(v) for k, v in dev.items()}]
+    sets_out = [(grad, loss, ws, sid), (torch.empty_like(grad), torch.empty_like(loss), torch.empty_like(ws),
+                                        torch.empty_like(sid))]
+    loss_host = [torch.empty(1, dtype=torch.float32, pin_memory=True) for _ in range(2)]
 
-    def e2e_step():
+    def e2e_h2d(bi):
         for k in host:
-            dev[k].copy_(pin[k], non_blocking=True)
-        s = pvl.pack_build_seq_ids(lay.seg_frames, lay.seg_valid, LOSS_GRID, L, out=sid)
-        pvl.masked_mse_loss(dev["pred"], dev["target"], s, grad=grad, loss=loss, ws=ws)
-        loss_host.copy_(loss, non_blocking=True)
+            sets_in[bi][k].copy_(pin[k], non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    def e2e_compute(bi):
+        g_, l_, w_, s_ = sets_out[bi]
+        pvl.pack_build_seq_ids(lay.seg_frames, lay.seg_valid, LOSS_GRID, L, out=s_)
+        pvl.masked_mse_loss(sets_in[bi]["pred"], sets_in[bi]["target"], s_, grad=g_, loss=l_, ws=w_)
+
+    def e2e_d2h(bi):
+        loss_host[bi].copy_(sets_out[bi][1], non_blocking=True)
+
+    e2e_steps = max(4, min(args.steps, 20))
+    pipelined_e2e(2, e2e_h2d, e2e_compute, e2e_d2h)
+    e2e_ms = pipelined_e2e(e2e_steps, e2e_h2d, e2e_compute, e2e_d2h)
     pvl.device_error()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, world) / e2e_steps
     peaks = load_peaks()
     hbm = peaks["hbm_gbs"]
     result = {
@@ -619,7 +676,8 @@ def run_loss(args):
                 "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in pin.values()),
                 "d2h_bytes_per_step": 4,
                 "note": "per step: pred and target copied in, seq_ids built from the host segment table, the "
-                        "loss call, the loss read back"},
+                        "loss call, the loss read back; neighbouring steps' copies overlap the compute (two buffer "
+                        "sets, three streams)"},
         "gpu_launches": 2 * args.steps,
         "roofline": {"kernel": "masked_mse_loss (count + loss kernels, timed together)", "bound": "hbm",
                      "achieved": round(bytes_step / (ms_step * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
