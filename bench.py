@@ -681,7 +681,8 @@ def run_loss(args):
         "gpu_launches": 2 * args.steps,
         "roofline": {"kernel": "masked_mse_loss (count + loss kernels, timed together)", "bound": "hbm",
                      "achieved": round(bytes_step / (ms_step * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(bytes_step / (ms_step * 1e-3) / 1e9 / hbm, 4), "traffic": None,
+                     "frac": round(bytes_step / (ms_step * 1e-3) / 1e9 / hbm, 4),
+                     "traffic": traffic_record("masked_loss.cu", "loss64k"),
                      "peak_note": f"of {peaks['source']} (STREAM-style copy)",
                      "algorithmic": "4 C per valid position + 2 C per position + 4 per id, bytes per launch pair"},
     }
