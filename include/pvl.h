@@ -344,6 +344,17 @@ PVL_API pvl_status masked_mse_loss_bwd(const pvl_bf16* pred, const pvl_bf16* tar
 PVL_API pvl_status pvl_device_error(pvl_stream_t stream);
 PVL_API pvl_status pvl_device_error_detail(pvl_stream_t stream, int32_t* info);
 
+/* pvl_selftest_wait_timeout — exercises the bounded waits every kernel uses,
+ * without a fault: one CTA in which warp 0 waits short_ns on an mbarrier
+ * that nothing arrives on (and records a timeout) while warp 1 waits up to
+ * long_ns on another and leaves through the CTA's abort flag.  Synchronises
+ * `stream`; out (host int32[2]) receives each warp's wait result (1 = the
+ * barrier completed, 0 = gave up: both 0 when the path works).  The timeout
+ * itself is then read with pvl_device_error (PVL_ERR_TIMEOUT, site 91).
+ * Errors: INVALID_ARG for a null out or limits outside 0 < short_ns <=
+ * long_ns, short_ns <= 10 s, long_ns <= 60 s; CUDA for launch failures. */
+PVL_API pvl_status pvl_selftest_wait_timeout(uint64_t short_ns, uint64_t long_ns, int32_t* out, pvl_stream_t stream);
+
 /* Human-readable text of the calling thread's last non-OK status. */
 PVL_API const char* pvl_last_error_message(void);
 

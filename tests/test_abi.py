@@ -81,6 +81,11 @@ def test_host_validation_without_gpu(lib):
     assert lib.adaln_bwd(dummy, dummy, dummy, 1, 4, 64, 1e-6, dummy, dummy, dummy, dummy, 0, null) == 1
     assert lib.adaln_bwd_ws_bytes(2, 100, 64) == 2 * (200 + 1) * 64 * 4      # a slot per (CTA, batch row)
     assert lib.adaln_bwd_ws_bytes(1, 64000, 5120) == 2 * 2048 * 5120 * 4     # at most 2048 CTAs
+    # bounded-wait self-test: argument checks only (no GPU here)
+    out2 = (ctypes.c_int32 * 2)()
+    assert lib.pvl_selftest_wait_timeout(0, 10, ctypes.addressof(out2), null) == 1
+    assert lib.pvl_selftest_wait_timeout(10, 5, ctypes.addressof(out2), null) == 1
+    assert lib.pvl_selftest_wait_timeout(10, 20, null, null) == 1
     # masked loss: C a multiple of 8, a finite grad_scale, a full workspace
     ws = lib.masked_mse_ws_bytes(1, 10, 8)
     assert ws > 0 and lib.masked_mse_ws_bytes(0, 10, 8) == 0
