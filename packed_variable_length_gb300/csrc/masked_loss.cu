@@ -20,11 +20,12 @@
 //     first block of data is in flight, adds the count to one 64-bit total
 //     (integer atomics: exact in any order) and arrives at a grid barrier (a
 //     bounded wait: on expiry the kernel records a timeout and returns);
-//   - after the barrier every CTA reads n_valid once, then streams its grid-stride share of 16-byte vectors: the token's id
-//     decides whether pred and target are read at all (padding tokens cost
-//     no reads), the squared error goes into a per-thread fp32 sum and the
-//     gradient is written in the same pass, the next block's ids fetched
-//     while the current block's data is in flight;
+//   - after the barrier every CTA reads n_valid once, then streams its
+//     grid-stride share of 16-byte vectors: the token's id decides whether
+//     pred and target are read at all (padding tokens cost no reads), the
+//     squared error goes into a per-thread fp32 sum and the gradient is
+//     written in the same pass, the next block's ids fetched while the
+//     current block's data is in flight;
 //   - CTA sums land in fp64 slots; the last CTA to finish adds them in CTA
 //     order, so the loss is deterministic for a given grid.
 #include <cuda_runtime.h>
