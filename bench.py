@@ -16,6 +16,9 @@ backward 10 D flops per pair and head).
 backward, `--workload loss64k` the frame_valid-masked loss with its gradient
 (both HBM bound, in GB/s).
 
+`--workload bucket_sweep` runs the same path over the 40 length-bucketed
+batches of 4 (160 episodes) in one step.
+
 `--workload cross_concat64k` (or cross_padded) measures cross attention
 instead: the same episodes as queries at 38 tokens per frame and as keys at 16
 tokens per frame, each side with its own seq_ids (12 launches per step: one
@@ -259,8 +262,8 @@ def cpu_baseline(lay, tensors, budget_heads=1, cl=None):
     dt = time.perf_counter() - t0
     flops = (FLOPS_PER_PAIR_FWD + FLOPS_PER_PAIR_BWD) * lay.D * len(heads) * unmasked_pairs(lay, Tk)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"fp64 numpy oracle, fwd+bwd of {len(heads)} of {lay.H} heads over all {lay.K} episodes "
-                      f"({lay.L} tokens), {dt:.1f} s; BLAS threads = host cores"}
+            "sample": f"fp64 numpy oracle, fwd+bwd of {len(heads)} of {lay.H} heads over all {lay.B * lay.K} episodes "
+                      f"({lay.B} x {lay.L} tokens), {dt:.1f} s; BLAS threads = host cores"}
 
 
 def run_gpu(args):
@@ -431,6 +434,200 @@ def run_gpu(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(lay, host, cl=cl)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------ bucket sweep workload
+def run_bucket_sweep(args):
+    """Workload 5: the 40 batches of 4 that the length-bucketing sampler cuts
+    from 160 episode lengths (F ~ U{103..362}, padded to multiples of 8, 38
+    tokens per frame, L = 38 F_pad per batch).  One step is the whole path
+    (seq_ids, tile map, forward, backward) over all 40 batches, in the
+    sampler's order; the metric is the headline's, over the sweep's unmasked
+    pairs.  Inputs: one seeded draw at the largest batch's size, each batch
+    reading its [4, L, H, D] prefix (values do not change the work)."""
+    import torch
+    import packed_variable_length_gb300 as pvl
+    import workloads as wl
+
+    rank, world, local = dist_setup(args.gpus)
+    layouts, batches, lengths = wl.bucket_sweep_layouts()
+    big = max(layouts, key=lambda la: la.B * la.L)
+    H, D, T = big.H, big.D, big.tokens_per_frame
+    host = wl.make_tensors(big)                               # bf16 CPU tensors, seeded
+    dev = {k: v.cuda().view(-1) for k, v in host.items()}
+    n_max = big.B * big.L * H * D
+    outs = {n: torch.empty(n_max, dtype=torch.bfloat16, device="cuda") for n in ("o", "dq", "dk", "dv")}
+    lse_pool = torch.empty(big.B * H * big.L, dtype=torch.float32, device="cuda")
+    sid_pool = torch.empty(big.B * big.L, dtype=torch.int32, device="cuda")
+    tm_pool = torch.empty(max(pvl.tile_map_ws_bytes(la.B, la.L) for la in layouts), dtype=torch.uint8, device="cuda")
+    bws_pool = torch.empty(max(pvl.masked_attn_bwd_ws_bytes(la.B, la.L, H, D) for la in layouts),
+                           dtype=torch.uint8, device="cuda")
+    pairs = [unmasked_pairs(la) for la in layouts]
+    flops_fwd = FLOPS_PER_PAIR_FWD * D * H * sum(pairs)
+    flops_bwd = FLOPS_PER_PAIR_BWD * D * H * sum(pairs)
+    flops = flops_fwd + flops_bwd
+    valid_tokens = sum(int(la.seg_valid.sum()) * T for la in layouts)
+    padded_tokens = sum(la.B * la.L for la in layouts)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def views(la, ins, outs_):
+        shp = (la.B, la.L, H, D)
+        n = la.B * la.L * H * D
+        i = {k: ins[k][:n].view(shp) for k in ("q", "k", "v", "do")}
+        o = {k: outs_[k][:n].view(shp) for k in ("o", "dq", "dk", "dv")}
+        o["lse"] = outs_["lse"][: la.B * H * la.L].view(la.B, H, la.L)
+        return i, o
+
+    def batch_step(la, ins, outs_, timers=None):
+        i, o = views(la, ins, outs_)
+        sid = sid_pool[: la.B * la.L].view(la.B, la.L)
+        pvl.pack_build_seq_ids(la.seg_frames, la.seg_valid, T, la.L, out=sid)
+        tm = pvl.tile_map_build(sid, ws=tm_pool[: pvl.tile_map_ws_bytes(la.B, la.L)])
+        if timers is not None:
+            timers[0].record(stream)
+        pvl.masked_attn_fwd(i["q"], i["k"], i["v"], sid, tm, o=o["o"], lse=o["lse"])
+        if timers is not None:
+            timers[1].record(stream)
+        pvl.masked_attn_bwd(i["q"], i["k"], i["v"], o["o"], i["do"], o["lse"], sid, tm, dq=o["dq"], dk=o["dk"],
+                            dv=o["dv"], ws=bws_pool[: pvl.masked_attn_bwd_ws_bytes(la.B, la.L, H, D)])
+        if timers is not None:
+            timers[2].record(stream)
+
+    dev_out = {**outs, "lse": lse_pool}
+
+    def step(timers=None):
+        for bi, la in enumerate(layouts):
+            batch_step(la, dev, dev_out, None if timers is None else timers[bi])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    pvl.device_error()
+    n_steps = max(1, min(args.steps, 10))     # one step is ~0.3 s of GPU work
+    timers = [[[ev(), ev(), ev()] for _ in layouts] for _ in range(n_steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start, t_end = ev(), ev()
+    t_start.record(stream)
+    for i in range(n_steps):
+        step(timers[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    pvl.device_error()
+    ms_step = max_over_ranks(t_start.elapsed_time(t_end), world) / n_steps
+    fwd_ms = sum(t[0].elapsed_time(t[1]) for st in timers for t in st) / n_steps
+    bwd_ms = sum(t[1].elapsed_time(t[2]) for st in timers for t in st) / n_steps
+
+    # end to end: each batch's inputs copied in from pinned host memory and its
+    # results copied back, neighbouring batches' copies overlapping the compute
+    pin = {k: v.view(-1).pin_memory() for k, v in host.items()}
+    sets_in = [dev, {k: torch.empty_like(v) for k, v in dev.items()}]
+    sets_out = [dev_out, {k: torch.empty_like(v) for k, v in dev_out.items()}]
+    out_host = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in so.items()} for so in sets_out]
+    cursor = {"h2d": 0, "compute": 0, "d2h": 0}
+
+    def nxt(kind):
+        la = layouts[cursor[kind] % len(layouts)]
+        cursor[kind] += 1
+        return la
+
+    def e2e_h2d(b):
+        la = nxt("h2d")
+        n = la.B * la.L * H * D
+        for k in ("q", "k", "v", "do"):
+            sets_in[b][k][:n].copy_(pin[k][:n], non_blocking=True)
+
+    def e2e_compute(b):
+        batch_step(nxt("compute"), sets_in[b], sets_out[b])
+
+    def e2e_d2h(b):
+        la = nxt("d2h")
+        n = la.B * la.L * H * D
+        for k in ("o", "dq", "dk", "dv"):
+            out_host[b][k][:n].copy_(sets_out[b][k][:n], non_blocking=True)
+        m = la.B * H * la.L
+        out_host[b]["lse"][:m].copy_(sets_out[b]["lse"][:m], non_blocking=True)
+
+    pipelined_e2e(2, e2e_h2d, e2e_compute, e2e_d2h)
+    for kind in cursor:
+        cursor[kind] = 0
+    barrier(world)
+    e2e_passes = 2
+    e2e_ms = max_over_ranks(pipelined_e2e(e2e_passes * len(layouts), e2e_h2d, e2e_compute, e2e_d2h), world) / e2e_passes
+    pvl.device_error()
+    h2d = sum(8 * la.B * la.L * H * D for la in layouts)
+    d2h = sum(8 * la.B * la.L * H * D + 4 * la.B * H * la.L for la in layouts)
+
+    # tile efficiency over the sweep: unmasked pairs / pairs inside computed tiles
+    tiles = {"fwd": 0, "bwd": 0}
+    for la in layouts:
+        sid = pvl.pack_build_seq_ids(la.seg_frames, la.seg_valid, T, la.L)
+        tmh = pvl.tile_map_build(sid)
+        for name, level, area in (("fwd", 1, 256 * 128), ("bwd", 0, 128 * 128)):
+            tiles[name] += int((tmh.to_host(level)["cls"] > 0).sum()) * area
+    tile_eff = {k: round(sum(pairs) / v, 4) for k, v in tiles.items()}
+    f_valid = sum(int(la.seg_valid.sum()) for la in layouts)
+    f_padded = sum(la.B * int(la.seg_frames[0, 0]) for la in layouts)
+
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+    value = aggregate(flops, ms_step, world) / 1e12
+    bwd_achieved = flops_bwd / (bwd_ms * 1e-3) / 1e12
+    n_launch = LAUNCHES_PER_STEP * len(layouts)
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": n_steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": (f"bucket_sweep: {len(layouts)} batches of 4 from the length-bucketing sampler over "
+                         f"{len(lengths)} episodes (F ~ U{{103..362}}, padded to multiples of 8, {T} tokens/frame), "
+                         f"L = {T} x F_pad per batch ({min(la.L for la in layouts)}..{max(la.L for la in layouts)}); "
+                         f"H = {H}, D = {D}; one step = all {len(layouts)} batches"),
+            "H": H, "D": D, "tokens_per_frame": T, "batches": len(layouts),
+            "distinct_shapes": len({la.L for la in layouts}),
+            "waste_pct": round(100.0 * (1 - f_valid / f_padded), 2),
+            "unmasked_pairs_per_head": sum(pairs), "tile_efficiency": tile_eff,
+            "step": "per batch: pack_build_seq_ids + tile_map_build + masked_attn_fwd + masked_attn_bwd",
+            "inputs": "one seeded draw at the largest batch's size; each batch reads its prefix",
+            "l2": "every batch's fwd + bwd touches more than L2 (Q, K, V, dO >= 52 MB each, fp32 dQ accumulator); "
+                  "no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "tokens_per_s": round(world * valid_tokens / (ms_step * 1e-3), 1),
+        "padded_tokens_per_s": round(world * padded_tokens / (ms_step * 1e-3), 1),
+        "pct_of_peak": round(100.0 * (value / world) / peak, 2), "peak_tflops": peak,
+        "peak_kind": f"bf16 dense, {peaks['source']} sustained",
+        "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
+        "fwd_tflops": round(flops_fwd / (fwd_ms * 1e-3) / 1e12, 2), "bwd_tflops": round(bwd_achieved, 2),
+        "clocks": clk,
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "every batch copies its Q, K, V, dO in from pinned host memory and O, LSE, dQ, dK, dV back; "
+                        "neighbouring batches' copies overlap the compute (two buffer sets, three streams)"},
+        "gpu_launches": n_launch * n_steps,
+        "roofline": {
+            "kernel": "masked_attn_bwd (bwd_pre + bwd_main + bwd_convert launches, timed together), summed over "
+                      "the 40 batches",
+            "bound": "tensor", "achieved": round(bwd_achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(bwd_achieved / peak, 4), "traffic": None,
+            "peak_note": f"of {peaks['source']} (bf16 cuBLAS, sustained)",
+            "algorithmic": "10 * D * H * unmasked pairs per launch",
+        },
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        small = min(layouts, key=lambda la: la.B * la.L)
+        result["cpu_baseline"] = cpu_baseline(small, wl.make_tensors(small), budget_heads=4)
+        result["cpu_baseline"]["sample"] += f" (batch {small.name}, the sweep's smallest)"
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -902,7 +1099,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="concat64k", choices=sorted(WORKLOADS) + ["adaln64k", "loss64k", "adaptive_load"],
+    ap.add_argument("--workload", default="concat64k", choices=sorted(WORKLOADS) + ["adaln64k", "loss64k", "adaptive_load", "bucket_sweep"],
                     help="concat64k is the headline workload; the others are smaller cases for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -916,6 +1113,8 @@ def main():
         run_loss(args)
     elif args.workload == "adaptive_load":
         run_adaptive(args)
+    elif args.workload == "bucket_sweep":
+        run_bucket_sweep(args)
     else:
         run_gpu(args)
 
