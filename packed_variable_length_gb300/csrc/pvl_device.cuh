@@ -23,8 +23,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
-
 // Error reporting: the first failing thread records (code, where, block);
 // every thread of the CTA sees the shared abort flag and leaves its loop.
 struct KernelCtl {
@@ -114,11 +112,6 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-// Named barrier over `nthreads` threads (whole warps) with id 1..15.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (TMA, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_async_smem() {
@@ -137,16 +130,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// 2-d tiled load (used by the building-block self test).
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
-                                            int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -180,9 +163,6 @@ __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.b
 
 // ----------------------------------------------------------------- tcgen05
 // TMEM address: bits 31..16 lane, bits 15..0 column.
-__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
-  return base + (lane << 16) + col;
-}
 
 // Whole warp: allocate `ncols` TMEM columns, base address written to smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
@@ -366,11 +346,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void red_add_v4(float* gptr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gptr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
 
