@@ -18,9 +18,12 @@
  *  - Pointers marked "dev" are device pointers of the current CUDA device;
  *    "host" pointers are ordinary host memory read before the call returns.
  *  - The caller owns and allocates every buffer and the stream.  The library
- *    allocates no device memory (its only device globals are a 16-byte error
- *    record per device).  Calls are asynchronous on `stream` (NULL = legacy
- *    default stream) and return after enqueueing.
+ *    allocates no device memory at run time.  Its static device globals, held
+ *    by every GPU that loads it until the process exits, are: a 16-byte error
+ *    record, the PVL_NO_ALLOC_SCRATCH_BYTES scratch array of
+ *    masked_attn_bwd_no_alloc, and two 32-bit result words of
+ *    pvl_selftest_wait_timeout.  Calls are asynchronous on `stream` (NULL =
+ *    legacy default stream) and return after enqueueing.
  *  - Arguments are validated on the host before anything is launched; a
  *    failed check returns a status and launches nothing.  Device-side
  *    failures (a bounded wait that ran out, a tile map built for another
@@ -247,7 +250,11 @@ PVL_API pvl_status masked_attn_bwd_cross(const pvl_bf16* q, const pvl_bf16* k, c
  *   PVL_ERR_UNSUPPORTED without launching anything.
  * Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept for the rest of the
+ *   process: it assumes the device keeps one CUDA context (the runtime's
+ *   primary context) for the life of the process; after a cudaDeviceReset
+ *   the kept address is stale and this call must not be used again.  The
+ *   error record that every call uses is located the same way.
  * Sharing: all calls on a device use the same array.  Each call clears what
  *   must start at zero, so earlier contents do not matter, but calls whose
  *   work overlaps on the GPU (other streams, other threads) race on the
@@ -356,6 +363,28 @@ PVL_API pvl_status pvl_device_error_detail(pvl_stream_t stream, int32_t* info);
  * Errors: INVALID_ARG for a null out or limits outside 0 < short_ns <=
  * long_ns, short_ns <= 10 s, long_ns <= 60 s; CUDA for launch failures. */
 PVL_API pvl_status pvl_selftest_wait_timeout(uint64_t short_ns, uint64_t long_ns, int32_t* out, pvl_stream_t stream);
+
+/* pvl_set_attn_wait_timeout_ns — the bound on any single device-side wait of
+ * the attention kernels (masked_attn_fwd*, masked_attn_bwd*) launched after
+ * this call, process-wide.  ns = 0 restores the default of 2 s; at most 60 s.
+ * A wait that runs out records PVL_ERR_TIMEOUT (read by pvl_device_error)
+ * and the kernel leaves through its abort path: every role stops, copies
+ * and MMAs in flight are drained, tensor memory is released and the kernel
+ * returns, so the context stays usable.  The outputs of such a call are
+ * undefined.  A bound far below the time a tile load takes (a few
+ * nanoseconds) makes the kernels' first waits run out: this is how the
+ * abort path is tested on a working GPU.  Errors: INVALID_ARG above 60 s. */
+PVL_API pvl_status pvl_set_attn_wait_timeout_ns(uint64_t ns);
+
+/* pvl_mark_next_bwd_main — for measurement: `before` and `after` (cudaEvent_t
+ * handles, created by the caller) are recorded on the call's stream just
+ * before and just after the launch of the main backward kernel of the calling
+ * thread's next masked_attn_bwd, masked_attn_bwd_cross or
+ * masked_attn_bwd_no_alloc call (the Delta / dQ-accumulator preprocess and
+ * the dQ conversion launches stay outside the pair), so that the main kernel
+ * can be timed alone.  One-shot: that call consumes and clears both; either
+ * may be null; null / null clears a pending pair.  Always PVL_OK. */
+PVL_API pvl_status pvl_mark_next_bwd_main(void* before, void* after);
 
 /* Human-readable text of the calling thread's last non-OK status. */
 PVL_API const char* pvl_last_error_message(void);

@@ -24,7 +24,9 @@ from .api import (  # noqa: F401
     masked_mse_loss,
     masked_mse_loss_bwd,
     masked_mse_ws_bytes,
+    mark_next_bwd_main,
     pack_build_seq_ids,
+    set_attn_wait_timeout_ns,
     tile_map_build,
     tile_map_ws_bytes,
     version,

@@ -43,6 +43,8 @@ SIGNATURES = {
     "masked_mse_loss": (_c_int, [_p, _p, _p, _c_int, _c_int, _c_int, _p, _p, _c_float, _p, _c_size, _p]),
     "masked_mse_loss_bwd": (_c_int, [_p, _p, _p, _c_int, _c_int, _c_int, _p, _p, _p, _c_size, _p]),
     "pvl_selftest_wait_timeout": (_c_int, [ctypes.c_uint64, ctypes.c_uint64, _p, _p]),
+    "pvl_set_attn_wait_timeout_ns": (_c_int, [ctypes.c_uint64]),
+    "pvl_mark_next_bwd_main": (_c_int, [_p, _p]),
     "pvl_device_error": (_c_int, [_p]),
     "pvl_device_error_detail": (_c_int, [_p, _p]),
     "pvl_last_error_message": (ctypes.c_char_p, []),

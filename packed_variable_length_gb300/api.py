@@ -416,5 +416,28 @@ def device_error(stream=None, raise_on_error: bool = True):
     return st, list(info)
 
 
+def set_attn_wait_timeout_ns(ns: int) -> None:
+    """Bound on any single device-side wait of the attention kernels launched
+    from now on, process-wide; 0 restores the default (2 s)."""
+    _check(_lib.load().pvl_set_attn_wait_timeout_ns(int(ns)))
+
+
+def _event_handle(ev) -> int | None:
+    if ev is None:
+        return None
+    handle = int(ev.cuda_event)
+    if handle == 0:
+        raise ValueError("the event has no CUDA event yet: record it once before passing it")
+    return handle
+
+
+def mark_next_bwd_main(before, after) -> None:
+    """Records the torch.cuda.Event objects ``before`` / ``after`` around the
+    main backward kernel of this thread's next masked_attn_bwd call (one-shot;
+    see pvl_mark_next_bwd_main).  Each event must have been recorded once
+    already, so that its CUDA event exists."""
+    _check(_lib.load().pvl_mark_next_bwd_main(_event_handle(before), _event_handle(after)))
+
+
 def version() -> int:
     return int(_lib.load().pvl_version())

@@ -599,7 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bar_acc_free);
     }
     // every dQ reduction of this warp has completed before the CTA leaves
+    // (after an abort the last reductions may not have been committed yet:
+    // commit them, so that the wait covers them too)
     if (lane == 0) {
+      bulk_commit_group();
       bulk_wait_group_all();
       if (pend_q >= 0) mbar_arrive(&bar_q_empty[pend_q]);
     }
@@ -628,6 +631,9 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
                       const void* tile_ws, int B, int L, int Lk, int H, float scale, pvl_bf16* dq, pvl_bf16* dk,
                       pvl_bf16* dv, void* ws, cudaStream_t stream) {
   // L: queries (Lq), Lk: keys
+  void* mark_before = nullptr;  // measurement events of this call, if any
+  void* mark_after = nullptr;
+  take_bwd_main_marks(&mark_before, &mark_after);
   CUtensorMap tq, tk, tv, tdo, tdq;
   pvl_status st = make_bhld_tensor_map(&tq, q, B, L, H, D);
   if (st == PVL_OK) st = make_bhld_tensor_map(&tk, k, B, Lk, H, D);
@@ -680,15 +686,23 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   prm.total_items = static_cast<long long>(prm.n_kt) * H;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.scale = scale;
-  prm.timeout_ns = kDefaultTimeoutNs;
+  prm.timeout_ns = attn_wait_timeout_ns();
   const int smem = BwdSmem<D>::kBytes;
   st = check_cuda(cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                   "masked_attn_bwd smem attribute");
   if (st != PVL_OK) return st;
   const long long grid = prm.total_items < sms ? prm.total_items : sms;
+  if (mark_before) {
+    st = check_cuda(cudaEventRecord(static_cast<cudaEvent_t>(mark_before), stream), "masked_attn_bwd marker");
+    if (st != PVL_OK) return st;
+  }
   bwd_main_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, prm);
   st = check_cuda(cudaGetLastError(), "masked_attn_bwd main launch");
   if (st != PVL_OK) return st;
+  if (mark_after) {
+    st = check_cuda(cudaEventRecord(static_cast<cudaEvent_t>(mark_after), stream), "masked_attn_bwd marker");
+    if (st != PVL_OK) return st;
+  }
 
   const long long n8 = rows * D / 8;
   bwd_convert_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(dq_acc, reinterpret_cast<__nv_bfloat16*>(dq), scale, n8);
@@ -754,7 +768,10 @@ void* g_no_alloc_ptr[64] = {};
 
 // Device address of the scratch array on the current device.  Host code only
 // sees a host-side stand-in under the array's name, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, once per device, with that device current.  The kept
+// address is that of the device's context when it was looked up (one primary
+// context per device for the life of the process; cudaDeviceReset would make
+// it stale).
 pvl_status no_alloc_scratch(void** out) {
   int dev = -1;
   pvl_status st = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");

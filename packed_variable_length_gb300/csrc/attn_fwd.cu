@@ -582,7 +582,7 @@ pvl_status launch_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   prm.n_pairs = B * tm.nTq;
   prm.total_items = static_cast<long long>(prm.n_pairs) * H;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  prm.timeout_ns = kDefaultTimeoutNs;
+  prm.timeout_ns = attn_wait_timeout_ns();
   const int smem = FwdSmem<D>::kBytes;
   st = check_cuda(cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                   "masked_attn_fwd smem attribute");

@@ -89,13 +89,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // Waits for the phase with the given parity to complete.  Gives up after
 // ctl.timeout_ns (records a timeout at `where`) or when another thread of the
 // CTA has aborted; returns false in both cases.  The abort flag and the clock
-// are looked at about once a millisecond at most (the suspension limit).
+// are looked at about once a millisecond at most (the suspension limit, or
+// the wait's whole bound when that is shorter).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const KernelCtl& ctl,
                                           uint32_t where) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  const uint32_t hint = ctl.timeout_ns < 1000000ull ? static_cast<uint32_t>(ctl.timeout_ns) : 1000000u;
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
     if (*ctl.abort) return false;
     if (global_timer_ns() - t0 > ctl.timeout_ns) {
       raise_error(ctl, kDevErrTimeout, where);

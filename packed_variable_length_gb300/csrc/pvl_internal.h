@@ -125,6 +125,13 @@ pvl_status fail(pvl_status s, const char* fmt, ...);
 pvl_status check_cuda(int err, const char* what);  // err is a cudaError_t
 DeviceError* device_error_record();                // current device, null on failure
 int sm_count();                                    // current device, 0 on failure
+// Bound on any single wait of the attention kernels launched now
+// (kDefaultTimeoutNs unless pvl_set_attn_wait_timeout_ns changed it).
+uint64_t attn_wait_timeout_ns();
+// Events (cudaEvent_t) to record just before and just after the main
+// backward kernel of the calling thread's next backward call, set by
+// pvl_mark_next_bwd_main; handing them out clears them.
+void take_bwd_main_marks(void** before, void** after);
 
 // Shared argument checks of the attention calls: null pointers and sizes
 // (INVALID_ARG), D, alignment and limits (UNSUPPORTED).

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -25,6 +26,10 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+
+std::atomic<uint64_t> g_attn_wait_ns{kDefaultTimeoutNs};
+thread_local void* t_mark_before = nullptr;
+thread_local void* t_mark_after = nullptr;
 
 int current_device() {
   int dev = -1;
@@ -68,6 +73,14 @@ int sm_count() {
     g_sms[dev] = n;
   }
   return g_sms[dev];
+}
+
+uint64_t attn_wait_timeout_ns() { return g_attn_wait_ns.load(std::memory_order_relaxed); }
+
+void take_bwd_main_marks(void** before, void** after) {
+  *before = t_mark_before;
+  *after = t_mark_after;
+  t_mark_before = t_mark_after = nullptr;
 }
 
 pvl_status validate_attn(const char* who, const void* const* ptrs, int nptrs, int B, int L, int H, int D,
@@ -192,6 +205,19 @@ extern "C" pvl_status pvl_device_error_detail(pvl_stream_t stream, int32_t* info
 }
 
 extern "C" pvl_status pvl_device_error(pvl_stream_t stream) { return pvl_device_error_detail(stream, nullptr); }
+
+extern "C" pvl_status pvl_set_attn_wait_timeout_ns(uint64_t ns) {
+  if (ns > 60000000000ull) return fail(PVL_ERR_INVALID_ARG, "pvl_set_attn_wait_timeout_ns: %llu ns exceeds 60 s",
+                                       static_cast<unsigned long long>(ns));
+  g_attn_wait_ns.store(ns == 0 ? kDefaultTimeoutNs : ns, std::memory_order_relaxed);
+  return PVL_OK;
+}
+
+extern "C" pvl_status pvl_mark_next_bwd_main(void* before, void* after) {
+  t_mark_before = before;
+  t_mark_after = after;
+  return PVL_OK;
+}
 
 extern "C" const char* pvl_last_error_message(void) { return t_message; }
 

@@ -86,6 +86,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.pvl_selftest_wait_timeout(0, 10, ctypes.addressof(out2), null) == 1
     assert lib.pvl_selftest_wait_timeout(10, 5, ctypes.addressof(out2), null) == 1
     assert lib.pvl_selftest_wait_timeout(10, 20, null, null) == 1
+    # attention wait bound: at most 60 s, 0 restores the default; event marks need no GPU to be set or cleared
+    assert lib.pvl_set_attn_wait_timeout_ns(61_000_000_000) == 1
+    assert lib.pvl_set_attn_wait_timeout_ns(0) == 0
+    assert lib.pvl_mark_next_bwd_main(null, null) == 0
     # masked loss: C a multiple of 8, a finite grad_scale, a full workspace
     ws = lib.masked_mse_ws_bytes(1, 10, 8)
     assert ws > 0 and lib.masked_mse_ws_bytes(0, 10, 8) == 0

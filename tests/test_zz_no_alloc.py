@@ -5,8 +5,10 @@ the library's static scratch array instead of a caller workspace.
 
 The call goes straight through the C ABI (ctypes) and its gradients are
 compared with those of masked_attn_bwd, the entry point that takes a
-workspace, within the parity tolerances, on two calls in a row (the second
-call finds the first call's contents in the shared scratch).  This file is
+workspace, and with the fp64 oracle, within the parity tolerances, on two
+calls in a row (the second call finds the first call's contents in the
+shared scratch).  The two entry points run the same kernels, so the oracle
+comparison is what would catch a fault they share.  This file is
 collected last, so a run that stops at the first failure has run every other
 test before it (GPU)."""
 
@@ -16,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 from attn_check import check_rows, to_np
 
@@ -51,15 +54,18 @@ def test_matches_workspace_entry_point_twice(pvl, seed, D):
     o, lse = pvl.masked_attn_fwd(q, k, v, sid, tm)
     ref = pvl.masked_attn_bwd(q, k, v, o, do, lse, sid, tm)
     pvl.device_error()
-    valid = sid.cpu().numpy() >= 0
+    s = sid.cpu().numpy()
+    valid = s >= 0
+    dQ, dK, dV, _ = oracle.attention_bwd(t["q"], t["k"], t["v"], t["do"], s)
     scale = 1.0 / np.sqrt(D)
     for call in range(2):
         outs = [torch.full_like(q, float("nan")) for _ in range(3)]
         st = call_no_alloc(lib, q, k, v, o, do, lse, sid, tm, scale, *outs)
         assert st == 0, lib.pvl_last_error_message().decode()
         pvl.device_error()
-        for name, got, want in zip(("dQ", "dK", "dV"), outs, ref):
+        for name, got, want, exact in zip(("dQ", "dK", "dV"), outs, ref, (dQ, dK, dV)):
             check_rows(f"{name} (call {call + 1})", to_np(got), to_np(want), valid)
+            check_rows(f"{name} (call {call + 1}, oracle)", to_np(got), exact, valid)
 
 
 def test_rejects_shapes_beyond_the_scratch(pvl):
