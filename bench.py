@@ -75,6 +75,129 @@ def unmasked_pairs(lay, tokens_per_frame_k=None) -> int:
 
 
 # ------------------------------------------------------------------ clocks
+class NvmlClockSampler:
+    """Samples the SM clock, the power draw and the active clock-event reasons
+    every 10 ms through NVML's read-only queries (libnvidia-ml.so.1 through
+    ctypes), so that a timed region of a fraction of a second still gets a
+    clock record.  The GPU is found by the PCI address torch reports for the
+    CUDA device.  Raises OSError where NVML is not usable."""
+
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    PERIOD_S = 0.01
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        props = torch.cuda.get_device_properties(cuda_index)
+        bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0".encode()
+        self.handle = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.handle)) != 0:
+            raise OSError(f"no NVML device at {bus.decode()}")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.lib, self.ct = lib, ctypes
+        self.samples: list[tuple[float, float, float, int]] = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+
+    def _one(self):
+        ct, lib, h = self.ct, self.lib, self.handle
+        sm, smax, mw, bits = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(sm)) != 0:      # NVML_CLOCK_SM
+            return
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ct.byref(smax))
+        lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw))
+        self.reasons_fn(h, ct.byref(bits))
+        self.samples.append((float(sm.value), float(smax.value), mw.value / 1000.0, int(bits.value)))
+
+    def _loop(self):
+        while not self.stop_flag.is_set():
+            self._one()
+            time.sleep(self.PERIOD_S)
+
+    def start(self):
+        self._one()
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def stop(self) -> dict:
+        self.stop_flag.set()
+        if self.thread:
+            self.thread.join(timeout=5)
+        self._one()
+        sm = [x[0] for x in self.samples]
+        reasons = sorted({name for x in self.samples for bit, name in self.REASON_BITS.items() if x[3] & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(x[1] for x in self.samples) if sm else None,
+                "reasons": reasons, "samples": len(sm),
+                "power_w_max": round(max(x[2] for x in self.samples), 1) if sm else None,
+                "source": "NVML every 10 ms over the timed region"}
+
+
+def clock_sampler(cuda_index: int):
+    """NVML sampler where NVML answers, else nvidia-smi at 200 ms."""
+    try:
+        return NvmlClockSampler(cuda_index)
+    except (OSError, AttributeError, RuntimeError):
+        return ClockSampler(cuda_index)
+
+
+def choose_peak(peaks: dict, clk: dict, region_s: float):
+    """The bf16 peak that applies to a timed region: the burst figure (cuBLAS
+    timed alone, at full clock) unless the region lasts a second or more AND
+    its clock record shows the power cap; then the sustained figure (cuBLAS
+    back to back for seconds under the power cap).  Returns (peak, kind, why)."""
+    capped = "sw_power_cap" in (clk.get("reasons") or [])
+    if region_s >= 1.0 and capped and peaks.get("bf16_tflops_sustained"):
+        return peaks["bf16_tflops_sustained"], "sustained", \
+            f"timed region {region_s:.2f} s with sw_power_cap active in its clock record"
+    why = f"timed region {region_s:.2f} s, " + ("shorter than 1 s" if capped else "no sw_power_cap sample") + \
+        f" (median SM clock {clk.get('sm_mhz')} MHz over {clk.get('samples')} samples)"
+    return peaks["bf16_tflops"], "burst", why
+
+
+def blas_info() -> str:
+    """The BLAS library numpy calls and its thread count, read from the
+    running process (threadpoolctl where installed, else numpy's build
+    configuration and the library's own thread query)."""
+    try:
+        from threadpoolctl import threadpool_info
+        libs = [d for d in threadpool_info() if d.get("user_api") == "blas"]
+        if libs:
+            return "; ".join(f"{d.get('internal_api')} {d.get('version')} ({os.path.basename(d.get('filepath', ''))}), "
+                             f"{d.get('num_threads')} threads" for d in libs)
+    except ImportError:
+        pass
+    name = "unknown"
+    try:
+        cfg = np.show_config(mode="dicts")
+        name = cfg["Build Dependencies"]["blas"].get("name", "unknown")
+    except Exception:  # noqa: BLE001 - best effort description
+        pass
+    threads = None
+    try:
+        import ctypes
+        with open("/proc/self/maps") as fh:
+            paths = sorted({ln.split()[-1] for ln in fh if "openblas" in ln.lower() and ln.split()[-1].startswith("/")})
+        for path in paths:
+            lib = ctypes.CDLL(path)
+            for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_", "openblas_get_num_threads"):
+                fn = getattr(lib, sym, None)
+                if fn is not None:
+                    threads = int(fn())
+                    break
+            if threads is not None:
+                break
+    except OSError:
+        pass
+    env = {k: os.environ[k] for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS") if k in os.environ}
+    return f"{name}, {threads if threads is not None else 'unknown'} threads" + (f" (env {env})" if env else "")
+
+
 class ClockSampler:
     """Samples nvidia-smi every 200 ms while running."""
 
@@ -128,7 +251,7 @@ class ClockSampler:
                 if val.lower().startswith("active"):
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi every 200 ms"}
 
 
 def pipelined_e2e(n_steps, h2d, compute, d2h):
@@ -213,8 +336,9 @@ def aggregate(units_per_rank: float, ms_per_step_max: float, world: int) -> floa
     return world * units_per_rank / (ms_per_step_max * 1e-3)
 
 
-def traffic_record(kernel_file: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+def traffic_record(kernel_file: str, workload: str, kernel: str | None = None):
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    matches the source: of the file's whole call, or of one kernel of it."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -225,6 +349,9 @@ def traffic_record(kernel_file: str, workload: str):
     entry = rec.get(kernel_file)
     if not entry or entry.get("source_sha") != sha or entry.get("workload") != workload:
         return None
+    if kernel is not None:
+        rw = entry.get("kernels", {}).get(kernel)
+        return None if rw is None else int(sum(rw))
     return entry.get("dram_bytes_per_launch")
 
 
@@ -263,7 +390,7 @@ def cpu_baseline(lay, tensors, budget_heads=1, cl=None):
     flops = (FLOPS_PER_PAIR_FWD + FLOPS_PER_PAIR_BWD) * lay.D * len(heads) * unmasked_pairs(lay, Tk)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": f"fp64 numpy oracle, fwd+bwd of {len(heads)} of {lay.H} heads over all {lay.B * lay.K} episodes "
-                      f"({lay.B} x {lay.L} tokens), {dt:.1f} s; BLAS threads = host cores"}
+                      f"({lay.B} x {lay.L} tokens), {dt:.1f} s; BLAS: {blas_info()}"}
 
 
 def run_gpu(args):
@@ -308,6 +435,7 @@ def run_gpu(args):
         pvl.masked_attn_fwd(dev["q"], dev["k"], dev["v"], sid, tm, o=o, lse=lse, k_seq_id=ksid)
         if timers is not None:
             timers[1].record(stream)
+            pvl.mark_next_bwd_main(timers[3], timers[4])   # the main backward kernel alone
         pvl.masked_attn_bwd(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, sid, tm, dq=dq, dk=dk, dv=dv, ws=bws,
                             k_seq_id=ksid)
         if timers is not None:
@@ -318,8 +446,12 @@ def run_gpu(args):
     torch.cuda.synchronize()
     pvl.device_error()
 
-    timers = [[ev(), ev(), ev()] for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    timers = [[ev() for _ in range(5)] for _ in range(args.steps)]
+    for t in timers:                # the library records [3], [4]: their CUDA events must exist
+        t[3].record(stream)
+        t[4].record(stream)
+    torch.cuda.synchronize()
+    clocks = clock_sampler(local)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
@@ -336,6 +468,7 @@ def run_gpu(args):
     ms_step = ms_total / args.steps
     fwd_ms = sum(t[0].elapsed_time(t[1]) for t in timers) / args.steps
     bwd_ms = sum(t[1].elapsed_time(t[2]) for t in timers) / args.steps
+    main_ms = sum(t[3].elapsed_time(t[4]) for t in timers) / args.steps
 
     # end to end: every step copies its inputs in from pinned host memory and
     # its results back, inside the timed region; neighbouring steps' copies
@@ -381,10 +514,12 @@ def run_gpu(args):
         tile_eff[name] = round(pairs / (int((cls > 0).sum()) * area), 4)
 
     peaks = load_peaks()
-    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+    peak, peak_kind, peak_why = choose_peak(peaks, clk, ms_total * 1e-3)
     value = aggregate(flops, ms_step, world) / 1e12
     bwd_achieved = flops_bwd / (bwd_ms * 1e-3) / 1e12
+    main_achieved = flops_bwd / (main_ms * 1e-3) / 1e12
     traffic = traffic_record("attn_bwd.cu", args.workload)
+    main_traffic = traffic_record("attn_bwd.cu", args.workload, f"bwd_main_kernel<{D}>")
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -413,11 +548,13 @@ def run_gpu(args):
         "padded_tokens_per_s": round(world * B * L / (ms_step * 1e-3), 1),
         "pct_of_peak": round(100.0 * (value / world) / peak, 2),
         "peak_tflops": peak,
-        "peak_kind": f"bf16 dense, {peaks['source']} sustained",
+        "peak_kind": f"bf16 dense, {peaks['source']} {peak_kind}: {peak_why}",
         "fwd_ms": round(fwd_ms, 4),
         "bwd_ms": round(bwd_ms, 4),
+        "bwd_main_ms": round(main_ms, 4),
         "fwd_tflops": round(flops_fwd / (fwd_ms * 1e-3) / 1e12, 2),
         "bwd_tflops": round(bwd_achieved, 2),
+        "bwd_main_tflops": round(main_achieved, 2),
         "clocks": clk,
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -425,11 +562,19 @@ def run_gpu(args):
                         "neighbouring steps' copies overlap the compute (two buffer sets, three streams)"},
         "gpu_launches": launches * args.steps,
         "roofline": {
+            "kernel": f"bwd_main_kernel<{D}> (the main backward launch alone, timed by its own CUDA events "
+                      "on the launching stream)",
+            "bound": "tensor", "achieved": round(main_achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(main_achieved / peak, 4), "traffic": main_traffic,
+            "peak_note": f"of {peaks['source']} (bf16 cuBLAS, {peak_kind})",
+            "algorithmic": "10 * D * H * unmasked pairs per launch",
+        },
+        "roofline_bwd_call": {
             "kernel": "masked_attn_bwd (bwd_pre + bwd_main + bwd_convert launches, timed together)",
             "bound": "tensor", "achieved": round(bwd_achieved, 2), "peak": peak, "unit": "TFLOP/s",
             "frac": round(bwd_achieved / peak, 4), "traffic": traffic,
-            "peak_note": f"of {peaks['source']} (bf16 cuBLAS, sustained)",
-            "algorithmic": "10 * D * H * unmasked pairs per launch",
+            "peak_note": f"of {peaks['source']} (bf16 cuBLAS, {peak_kind})",
+            "algorithmic": "10 * D * H * unmasked pairs per call",
         },
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -511,7 +656,7 @@ def run_bucket_sweep(args):
     pvl.device_error()
     n_steps = max(1, min(args.steps, 10))     # one step is ~0.3 s of GPU work
     timers = [[[ev(), ev(), ev()] for _ in layouts] for _ in range(n_steps)]
-    clocks = ClockSampler(local)
+    clocks = clock_sampler(local)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
@@ -524,7 +669,8 @@ def run_bucket_sweep(args):
     barrier(world)
     clk = clocks.stop()
     pvl.device_error()
-    ms_step = max_over_ranks(t_start.elapsed_time(t_end), world) / n_steps
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world)
+    ms_step = ms_total / n_steps
     fwd_ms = sum(t[0].elapsed_time(t[1]) for st in timers for t in st) / n_steps
     bwd_ms = sum(t[1].elapsed_time(t[2]) for st in timers for t in st) / n_steps
 
@@ -580,7 +726,7 @@ def run_bucket_sweep(args):
     f_padded = sum(la.B * int(la.seg_frames[0, 0]) for la in layouts)
 
     peaks = load_peaks()
-    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+    peak, peak_kind, peak_why = choose_peak(peaks, clk, ms_total * 1e-3)
     value = aggregate(flops, ms_step, world) / 1e12
     bwd_achieved = flops_bwd / (bwd_ms * 1e-3) / 1e12
     n_launch = LAUNCHES_PER_STEP * len(layouts)
@@ -606,7 +752,7 @@ def run_bucket_sweep(args):
         "tokens_per_s": round(world * valid_tokens / (ms_step * 1e-3), 1),
         "padded_tokens_per_s": round(world * padded_tokens / (ms_step * 1e-3), 1),
         "pct_of_peak": round(100.0 * (value / world) / peak, 2), "peak_tflops": peak,
-        "peak_kind": f"bf16 dense, {peaks['source']} sustained",
+        "peak_kind": f"bf16 dense, {peaks['source']} {peak_kind}: {peak_why}",
         "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
         "fwd_tflops": round(flops_fwd / (fwd_ms * 1e-3) / 1e12, 2), "bwd_tflops": round(bwd_achieved, 2),
         "clocks": clk,
@@ -620,7 +766,7 @@ def run_bucket_sweep(args):
                       "the 40 batches",
             "bound": "tensor", "achieved": round(bwd_achieved, 2), "peak": peak, "unit": "TFLOP/s",
             "frac": round(bwd_achieved / peak, 4), "traffic": None,
-            "peak_note": f"of {peaks['source']} (bf16 cuBLAS, sustained)",
+            "peak_note": f"of {peaks['source']} (bf16 cuBLAS, {peak_kind})",
             "algorithmic": "10 * D * H * unmasked pairs per launch",
         },
     }
@@ -680,7 +826,7 @@ def run_adaln(args):
     torch.cuda.synchronize()
     pvl.device_error()
     timers = [[ev(), ev(), ev()] for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    clocks = clock_sampler(local)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
@@ -814,7 +960,7 @@ def run_loss(args):
     torch.cuda.synchronize()
     pvl.device_error()
     pairs = [(ev(), ev()) for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    clocks = clock_sampler(local)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
@@ -924,10 +1070,14 @@ def run_adaptive(args):
          memory-bound batch) are batched three ways:
          equal-token (B = floor(M_mem / S)), dual-constraint (B_shape), and
          the fixed batch of 4 of the packing report's sampler.
-      3. Every batch's layer step is timed; reported per arm: the coefficient
-         of variation of the batch step times (the page's imbalance measure)
-         and the valid tokens/s of 8 simulated synchronous data-parallel ranks
-         taking the batches round-robin (each step as long as its slowest)."""
+      3. Every batch's layer step is timed; reported per arm, under the
+         page's names ("AdaptiveLoad" §4, load-balance results): the
+         compute imbalance rate, the coefficient of variation of the batches'
+         compute load (here the fitted cost model's load B S^p), and the
+         synchronisation overhead, the coefficient of variation of the step
+         time (here the measured batch step times); plus the valid tokens/s
+         of 8 simulated synchronous data-parallel ranks taking the batches
+         round-robin (each step as long as its slowest)."""
     import torch
     import packed_variable_length_gb300 as pvl
     from packed_variable_length_gb300 import adaptive_load as al
@@ -983,7 +1133,7 @@ def run_adaptive(args):
         torch.cuda.synchronize()
         return float(np.median([a.elapsed_time(b) for a, b in pairs])) * 1e-3
 
-    clocks = ClockSampler(local)
+    clocks = clock_sampler(local)
     clocks.start()
     # 1. shape benchmarking and the cost-model fit
     shapes = [(Bn, fp) for fp in (104, 168, 232, 296, 360) for Bn in (1, 2, 4, 8, 16) if Bn * T * fp <= n_max]
@@ -1014,8 +1164,9 @@ def run_adaptive(args):
             loads.append(len(bt) * (T * fp) ** model.p)
             n_launch += 11 * 4
         tps, step_t, idle = al.simulate_data_parallel(times, tokens, ADAPTIVE_RANKS)
-        results[name] = {"batches": len(batches), "cv_step_time": round(al.coefficient_of_variation(times), 4),
-                         "cv_modelled_load": round(al.coefficient_of_variation(loads), 4),
+        results[name] = {"batches": len(batches),
+                         "compute_imbalance_rate_cv_modelled_load": round(al.coefficient_of_variation(loads), 4),
+                         "sync_overhead_cv_step_time": round(al.coefficient_of_variation(times), 4),
                          "sim_dp8_tokens_per_s": round(tps, 1), "sim_dp8_idle_fraction": round(idle, 4),
                          "sim_dp8_cv_step": round(al.coefficient_of_variation(step_t), 4),
                          "batch_sizes": sorted(set(len(b) for b in batches)),
@@ -1038,6 +1189,15 @@ def run_adaptive(args):
                                   "shapes": len(shapes)},
                    "m_comp": m_comp, "s_ref": s_min, "arms": results,
                    "dual_vs_equal_token_throughput": round(dual["sim_dp8_tokens_per_s"] / base["sim_dp8_tokens_per_s"], 4),
+                   "page_measures": {
+                       "compute imbalance rate (CV of compute load)": {
+                           "here_equal_token_to_dual": [base["compute_imbalance_rate_cv_modelled_load"],
+                                                        dual["compute_imbalance_rate_cv_modelled_load"]],
+                           "page": "39% -> 18.9% (its corpus and cluster)"},
+                       "synchronisation overhead (CV of step time)": {
+                           "here_equal_token_to_dual": [base["sync_overhead_cv_step_time"],
+                                                        dual["sync_overhead_cv_step_time"]],
+                           "page": "18.7% -> 10.4% (16 GPUs)"}},
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "clocks": clk,
         "gpu_launches": n_launch,
@@ -1091,7 +1251,8 @@ def run_reference(args):
     cores = len(os.sched_getaffinity(0))
     sample = (f"fp64 numpy oracle: each step is fwd+bwd of one block of <= {block} queries of one (episode, head) "
               f"of the concat64k workload against all of that episode's keys ({len(samples)} blocks over {lay.K} "
-              f"episodes x {lay.H} heads, seeded order); {args.steps} timed steps, {done_time:.1f} s")
+              f"episodes x {lay.H} heads, seeded order); {args.steps} timed steps, {done_time:.1f} s; "
+              f"BLAS: {blas_info()}")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * done_time / args.steps,
