@@ -206,7 +206,8 @@ PVL_API pvl_status masked_attn_fwd_cross(const pvl_bf16* q, const pvl_bf16* k, c
  * seq_id -1 get exact zeros.
  * ws: dev scratch of masked_attn_bwd_ws_bytes(B, L, H, D) bytes, 256-byte
  *   aligned (fp32 dQ accumulator; Delta, LSE*log2(e) and query seq_ids padded
- *   to whole 128-row tiles); contents on entry are ignored.
+ *   to whole 128-row tiles; the counter that hands out work items); contents
+ *   on entry are ignored.  A workspace serves one call at a time.
  * Errors: as masked_attn_fwd, plus INVALID_ARG for a short workspace.
  * ---------------------------------------------------------------------- */
 PVL_API size_t masked_attn_bwd_ws_bytes(int B, int L, int H, int D);

@@ -12,12 +12,15 @@
 //
 // Three launches on the caller's stream:
 //   bwd_pre      Delta and LSE * log2(e) per query (fp32, padded to whole
-//                128-row tiles), the padded query seq_ids, and a zeroed fp32
-//                dQ accumulator;
+//                128-row tiles), the padded query seq_ids, a zeroed fp32
+//                dQ accumulator and a zeroed work-item counter;
 //   bwd_main     one persistent CTA per SM over work items (b, key tile, head)
 //                in the tile map's longest-first key order, head-major (the
 //                CTAs working at one time add into one head's dQ rows, which
-//                stay in L2).  Per item the K/V
+//                stay in L2).  Items are handed out at run time from a
+//                counter in the workspace, so a CTA that finishes early takes
+//                the next one (items differ in length; a fixed round-robin
+//                share left the CTAs 5-20 % apart).  Per item the K/V
 //                tile stays in shared memory while the non-empty query tiles
 //                stream through (FULL first, PARTIAL last), Q in a 2-stage
 //                ring, dO with the tile's LSE / Delta / seq_id rows in one:
@@ -64,8 +67,14 @@ constexpr uint32_t kColDV = 256;  // dV             [256, 256 + D)
 
 enum BwdSite : uint32_t {
   kSiteKvEmpty = 21, kSiteQdoEmpty, kSiteKvFull, kSiteQdoFull, kSiteDqFree, kSitePsFull, kSiteAccFree,
-  kSiteSFull, kSiteDpFull, kSiteMmaDone, kSiteDqReady, kSiteDoEmpty, kSiteDoFull, kSiteDoFullC
+  kSiteSFull, kSiteDpFull, kSiteMmaDone, kSiteDqReady, kSiteDoEmpty, kSiteDoFull, kSiteDoFullC, kSiteItemEmpty,
+  kSiteItemFull
 };
+
+// Work items are handed out at run time: the producer thread takes the next
+// item index from a global counter (atomicAdd) and passes it to the MMA and
+// compute warps through a ring of this many shared-memory slots.
+constexpr int kItemSlots = 2;
 
 template <int D>
 struct BwdSmem {
@@ -94,6 +103,7 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   DeviceError* err;
+  unsigned int* sched;  // work-item counter, zero at launch
   int B, Lq, Lk, Lp, H;
   int nT;   // key tiles per row (items)
   int nTq;  // query tiles per row: the length of each key tile's query list
@@ -121,10 +131,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       const __nv_bfloat16* __restrict__ dO,
                                                       const float* __restrict__ lse, const int32_t* __restrict__ seq_id,
                                                       float* __restrict__ delta, float* __restrict__ lse2,
-                                                      int32_t* __restrict__ qseq, float* __restrict__ dq_acc, int B,
-                                                      int L, int Lp, int H) {
+                                                      int32_t* __restrict__ qseq, float* __restrict__ dq_acc,
+                                                      unsigned int* __restrict__ sched, int B, int L, int Lp, int H) {
   constexpr int G = D / 8;
   const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0u;  // the main kernel's work-item counter
   const long long rows = static_cast<long long>(B) * L * H;
   const long long total = rows * G;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;  // a multiple of 32
@@ -256,6 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float lse2_s[128];
   __shared__ __align__(16) float delta_s[128];
   __shared__ __align__(16) int32_t qseq_s[128];
+  __shared__ int item_s[kItemSlots];
+  __shared__ uint64_t bar_item_full[kItemSlots], bar_item_empty[kItemSlots];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -292,6 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_dq_free, kComputeThreads);
     mbar_init(&bar_acc_free, kComputeThreads);
     mbar_init(&bar_final, 1);
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(&bar_item_full[s], 1);                        // the producer thread
+      mbar_init(&bar_item_empty[s], 1 + kComputeThreads / 32);  // the MMA warp and each compute warp
+    }
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -326,7 +343,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
       return __shfl_sync(0xffffffffu, ok, 0);
     };
-    for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+    for (uint32_t it = 0; alive; ++it) {
+      // take the next work item and pass it on (-1: none left)
+      const int slot = it % kItemSlots;
+      if (!wait1(&bar_item_empty[slot], ((it / kItemSlots) & 1) ^ 1, kSiteItemEmpty)) { alive = false; break; }
+      if (lane == 0) {
+        const unsigned int t = atomicAdd(p.sched, 1u);
+        item_s[slot] = t < static_cast<unsigned long long>(p.total_items) ? static_cast<int>(t) : -1;
+        mbar_arrive(&bar_item_full[slot]);
+      }
+      __syncwarp();
+      const long long w = item_s[slot];
+      if (w < 0) break;
       const int tile = p.k_order[w % p.n_kt];
       const int h = static_cast<int>(w / p.n_kt);
       const int b = tile / nT, kt = tile % nT;
@@ -392,7 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto ready2 = [&](uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
       return __all_sync(0xffffffffu, mbar_try_wait(b0, p0) & mbar_try_wait(b1, p1));
     };
-    for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+    for (uint32_t it = 0; alive; ++it) {
+      const int slot = it % kItemSlots;
+      if (!wait1(&bar_item_full[slot], (it / kItemSlots) & 1, kSiteItemFull)) { alive = false; break; }
+      const long long w = item_s[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_item_empty[slot]);
+      if (w < 0) break;
       const int tile = p.k_order[w % p.n_kt];
       const int n = p.col_count[tile];
       if (n == 0) continue;
@@ -475,7 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto waitw = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
     };
-    for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+    for (uint32_t it = 0; alive; ++it) {
+      const int slot = it % kItemSlots;
+      if (!waitw(&bar_item_full[slot], (it / kItemSlots) & 1, kSiteItemFull)) { alive = false; break; }
+      const long long w = item_s[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_item_empty[slot]);
+      if (w < 0) break;
       const int tile = p.k_order[w % p.n_kt];
       const int h = static_cast<int>(w / p.n_kt);
       const int b = tile / nT, kt = tile % nT;
@@ -652,11 +692,12 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   float* delta = reinterpret_cast<float*>(wsb + bwd_ws_dq_bytes(B, L, H, D));
   float* lse2 = reinterpret_cast<float*>(wsb + bwd_ws_dq_bytes(B, L, H, D) + bwd_ws_rows_bytes(B, L, H));
   int32_t* qseq = reinterpret_cast<int32_t*>(wsb + bwd_ws_dq_bytes(B, L, H, D) + 2 * bwd_ws_rows_bytes(B, L, H));
+  unsigned int* sched = reinterpret_cast<unsigned int*>(wsb + bwd_ws_sched_offset(B, L, H, D));
   const long long rows = static_cast<long long>(B) * L * H;
 
   bwd_pre_kernel<D><<<grid_for(rows * (D / 8), 256), 256, 0, stream>>>(
       reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), lse, q_seq, delta, lse2,
-      qseq, dq_acc, B, L, Lp, H);
+      qseq, dq_acc, sched, B, L, Lp, H);
   st = check_cuda(cudaGetLastError(), "masked_attn_bwd preprocess launch");
   if (st != PVL_OK) return st;
 
@@ -675,6 +716,7 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   prm.dk = reinterpret_cast<__nv_bfloat16*>(dk);
   prm.dv = reinterpret_cast<__nv_bfloat16*>(dv);
   prm.err = err;
+  prm.sched = sched;
   prm.B = B;
   prm.Lq = L;
   prm.Lk = Lk;

@@ -14,8 +14,9 @@
 // head): two adjacent 128-row query tiles A and B that share one stream of
 // key tiles, taken from level 1 of the tile map (256-row query tiles) in its
 // longest-first order, head-major (the CTAs running together read one
-// head's K and V, 34 MB at 64k tokens, which stay in L2), round-robin over
-// CTAs.  Only the key tiles the map
+// head's K and V, 34 MB at 64k tokens, which stay in L2).  Items are handed
+// out at run time from a per-stream counter, so a CTA that finishes early
+// takes the next one (a fixed round-robin share left the CTAs 5-16 % apart).  Only the key tiles the map
 // lists as non-empty are touched, FULL ones first (no per-element mask),
 // then PARTIAL ones (mask from the seq_ids).
 //   warp 8      TMA producer: the Q pair once per item, K and V tiles into
@@ -66,8 +67,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum FwdSite : uint32_t {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull, kSitePFull, kSiteOFree,
-  kSiteSFull, kSitePvDone, kSiteTurn
+  kSiteSFull, kSitePvDone, kSiteTurn, kSiteItemEmpty, kSiteItemFull
 };
+
+// Work items are handed out at run time: the producer thread takes the next
+// item index from a counter (atomicAdd) and passes it to the MMA and softmax
+// warps through a ring of this many shared-memory slots.
+constexpr int kItemSlots = 2;
 
 template <int D>
 struct FwdSmem {
@@ -92,6 +98,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   DeviceError* err;
+  unsigned int* sched;       // work-item counter, zero at launch; null: fixed round-robin
   int B, Lq, Lk, H, nP, nK;  // query-tile pairs and key tiles per row
   long long total_items;  // n_pairs * H, head-major
   int n_pairs;            // B * nP: entries of the longest-first query-tile-pair order
@@ -208,6 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_o_free[2], bar_final[2], bar_turn[2];
   __shared__ uint64_t bar_k_full[kStages], bar_k_empty[kStages], bar_v_full[kStages], bar_v_empty[kStages];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2];
+  __shared__ int item_s[kItemSlots];
+  __shared__ uint64_t bar_item_full[kItemSlots], bar_item_empty[kItemSlots];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -244,6 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_p_full[x], 128);
       mbar_init(&bar_pv_done[x], 1);
     }
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(&bar_item_full[s], 1);      // the producer thread
+      mbar_init(&bar_item_empty[s], 2 + 8);  // both MMA warps and each softmax warp
+    }
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -279,7 +292,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = lane == 0 ? mbar_wait(bar, parity, ctl, site) : true;
         return __shfl_sync(0xffffffffu, ok, 0);
       };
-      for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+      for (uint32_t it = 0; alive; ++it) {
+        // take the next work item and pass it on (-1: none left)
+        const int slot = it % kItemSlots;
+        if (!wait1(&bar_item_empty[slot], ((it / kItemSlots) & 1) ^ 1, kSiteItemEmpty)) { alive = false; break; }
+        if (lane == 0) {
+          const unsigned long long t = p.sched ? atomicAdd(p.sched, 1u)
+                                               : blockIdx.x + static_cast<unsigned long long>(it) * gridDim.x;
+          item_s[slot] = t < static_cast<unsigned long long>(p.total_items) ? static_cast<int>(t) : -1;
+          mbar_arrive(&bar_item_full[slot]);
+        }
+        __syncwarp();
+        const long long w = item_s[slot];
+        if (w < 0) break;
         const int tile = p.q_order[w % p.n_pairs];
         const int h = static_cast<int>(w / p.n_pairs);
         const int b = tile / nP, pp = tile % nP;
@@ -377,7 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bar_pv_done[x]);
         umma_commit(&bar_v_empty[idx % kStages]);
       };
-      for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+      for (uint32_t it = 0; alive; ++it) {
+        const int slot = it % kItemSlots;
+        if (!wait1(&bar_item_full[slot], (it / kItemSlots) & 1, kSiteItemFull)) { alive = false; break; }
+        const long long w = item_s[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_item_empty[slot]);
+        if (w < 0) break;
         const int tile = p.q_order[w % p.n_pairs];
         const int n = p.row_count[tile];
         if (n == 0) continue;
@@ -443,7 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto waitw = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
     };
-    for (long long w = blockIdx.x; w < p.total_items && alive; w += gridDim.x) {
+    for (uint32_t it = 0; alive; ++it) {
+      const int slot = it % kItemSlots;
+      if (!waitw(&bar_item_full[slot], (it / kItemSlots) & 1, kSiteItemFull)) { alive = false; break; }
+      const long long w = item_s[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_item_empty[slot]);
+      if (w < 0) break;
       const int tile = p.q_order[w % p.n_pairs];
       const int h = static_cast<int>(w / p.n_pairs);
       const int b = tile / nP, pp = tile % nP;
@@ -583,6 +620,11 @@ pvl_status launch_fwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   prm.total_items = static_cast<long long>(prm.n_pairs) * H;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.timeout_ns = attn_wait_timeout_ns();
+  prm.sched = fwd_sched_counter(stream);
+  if (prm.sched) {
+    st = check_cuda(cudaMemsetAsync(prm.sched, 0, sizeof(unsigned int), stream), "masked_attn_fwd counter reset");
+    if (st != PVL_OK) return st;
+  }
   const int smem = FwdSmem<D>::kBytes;
   st = check_cuda(cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                   "masked_attn_fwd smem attribute");

@@ -128,6 +128,12 @@ int sm_count();                                    // current device, 0 on failu
 // Bound on any single wait of the attention kernels launched now
 // (kDefaultTimeoutNs unless pvl_set_attn_wait_timeout_ns changed it).
 uint64_t attn_wait_timeout_ns();
+// Device address of the forward's work-item counter for `stream` on the
+// current device: one slot per (device, stream), so that calls on one stream
+// (ordered) share it and calls on different streams do not.  The forward
+// zeroes it on the stream before each launch.  Null when the slots are all
+// taken (the forward then hands out its items in a fixed round-robin).
+unsigned int* fwd_sched_counter(void* stream);
 // Events (cudaEvent_t) to record just before and just after the main
 // backward kernel of the calling thread's next backward call, set by
 // pvl_mark_next_bwd_main; handing them out clears them.
@@ -143,7 +149,8 @@ pvl_status validate_attn_qk(const char* who, const void* const* ptrs, int nptrs,
 // Backward workspace, each part 256-byte aligned: the fp32 dQ accumulator
 // [B, L, H, D]; then, over query positions padded to whole 128-row tiles
 // (Lp), Delta and LSE * log2(e) as fp32 [B, H, Lp] and the query seq_ids as
-// int32 [B, Lp] (padding positions hold 0, 0 and -1).
+// int32 [B, Lp] (padding positions hold 0, 0 and -1); then the main
+// kernel's work-item counter (one uint32, zeroed by the preprocess).
 inline int bwd_lp(int L) { return ((L + 127) / 128) * 128; }
 inline size_t bwd_ws_dq_bytes(int B, int L, int H, int D) {
   return align256(static_cast<size_t>(B) * L * H * D * 4);
@@ -151,10 +158,11 @@ inline size_t bwd_ws_dq_bytes(int B, int L, int H, int D) {
 inline size_t bwd_ws_rows_bytes(int B, int L, int H) {
   return align256(static_cast<size_t>(B) * H * bwd_lp(L) * 4);
 }
-inline size_t bwd_ws_total_bytes(int B, int L, int H, int D) {
+inline size_t bwd_ws_sched_offset(int B, int L, int H, int D) {
   return bwd_ws_dq_bytes(B, L, H, D) + 2 * bwd_ws_rows_bytes(B, L, H) +
          align256(static_cast<size_t>(B) * bwd_lp(L) * 4);
 }
+inline size_t bwd_ws_total_bytes(int B, int L, int H, int D) { return bwd_ws_sched_offset(B, L, H, D) + 256; }
 
 // bf16 [B, L, H, D] tensor map with a (64 x 1 x 128 x 1) box and 128-byte
 // swizzle: one box is 128 rows of 64 features (16 KB).

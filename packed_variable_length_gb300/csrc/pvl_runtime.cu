@@ -7,13 +7,20 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <thread>
+#include <unordered_map>
 
 #include "pvl_internal.h"
 
 namespace pvl {
 
 __device__ DeviceError g_device_error;
+
+// Work-item counters of the forward, one per (device, stream) in use.
+constexpr int kSchedSlots = 256;
+__device__ unsigned int g_fwd_sched[kSchedSlots];
 
 namespace {
 thread_local char t_message[512] = "ok";
@@ -28,6 +35,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 EncodeTiledFn g_encode = nullptr;
 
 std::atomic<uint64_t> g_attn_wait_ns{kDefaultTimeoutNs};
+unsigned int* g_sched_base[kMaxDevices] = {};
+std::unordered_map<uintptr_t, int> g_sched_slot[kMaxDevices];
 thread_local void* t_mark_before = nullptr;
 thread_local void* t_mark_after = nullptr;
 
@@ -76,6 +85,29 @@ int sm_count() {
 }
 
 uint64_t attn_wait_timeout_ns() { return g_attn_wait_ns.load(std::memory_order_relaxed); }
+
+unsigned int* fwd_sched_counter(void* stream) {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  uintptr_t key = reinterpret_cast<uintptr_t>(stream);
+  // the per-thread default stream is one handle for a different stream in
+  // every host thread
+  if (stream == reinterpret_cast<void*>(cudaStreamPerThread))
+    key ^= std::hash<std::thread::id>{}(std::this_thread::get_id()) << 4;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_sched_base[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fwd_sched) != cudaSuccess) return nullptr;
+    g_sched_base[dev] = static_cast<unsigned int*>(p);
+  }
+  auto& slots = g_sched_slot[dev];
+  const auto found = slots.find(key);
+  if (found != slots.end()) return g_sched_base[dev] + found->second;
+  if (static_cast<int>(slots.size()) >= kSchedSlots) return nullptr;
+  const int slot = static_cast<int>(slots.size());
+  slots.emplace(key, slot);
+  return g_sched_base[dev] + slot;
+}
 
 void take_bwd_main_marks(void** before, void** after) {
   *before = t_mark_before;
