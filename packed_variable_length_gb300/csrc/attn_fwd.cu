@@ -60,6 +60,8 @@ constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;    // MMA issuer of query tile A; owns TMEM
 constexpr int kMmaWarpB = 10;  // MMA issuer of query tile B
 constexpr int kStages = 2;
+// MMAs of a bracket issued after the turn has passed to the other issuer
+constexpr int kTurnEarly = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S_X at [128 X, 128 X + 128); P_X packed over its first 64 columns
 constexpr uint32_t kColO = 256;  // O_X at [256 + X D, 256 + (X + 1) D)
@@ -385,20 +387,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
       const uint32_t qbase = sQ + x * kTileBytes;
-      auto issue_s = [&](uint32_t idx) {  // S_x = Q_x K^T (K stage of key tile idx)
+      // The K steps [k0, k1) of S_x = Q_x K^T (K stage of key tile idx).
+      auto issue_s = [&](uint32_t idx, int k0, int k1) {
         const uint32_t kbase = sK0 + (idx % kStages) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColS + x * 128, kmajor_desc(qbase, kk), kmajor_desc(kbase, kk), idesc_s, kk > 0 ? 1u : 0u);
+          if (kk >= k0 && kk < k1)
+            umma_ss(tmem + kColS + x * 128, kmajor_desc(qbase, kk), kmajor_desc(kbase, kk), idesc_s, kk > 0 ? 1u : 0u);
+      };
+      auto commit_s = [&](uint32_t idx) {
         umma_commit(&bar_s_full[x]);
         umma_commit(&bar_k_empty[idx % kStages]);
       };
-      auto issue_pv = [&](uint32_t idx, bool accumulate) {  // O_x += P_x V (P_x in TMEM)
+      // The K steps [k0, k1) of O_x += P_x V (P_x in TMEM).
+      auto issue_pv = [&](uint32_t idx, bool accumulate, int k0, int k1) {
         const uint32_t vbase = sV0 + (idx % kStages) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kColO + x * D, tmem + kColS + x * 128 + kk * 8, mnmajor_desc(vbase, kk), idesc_o,
-                  (accumulate || kk > 0) ? 1u : 0u);
+          if (kk >= k0 && kk < k1)
+            umma_ts(tmem + kColO + x * D, tmem + kColS + x * 128 + kk * 8, mnmajor_desc(vbase, kk), idesc_o,
+                    (accumulate || kk > 0) ? 1u : 0u);
+      };
+      auto commit_pv = [&](uint32_t idx) {
         umma_commit(&bar_pv_done[x]);
         umma_commit(&bar_v_empty[idx % kStages]);
       };
@@ -418,7 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait1(&bar_k_full[base % kStages], (base / kStages) & 1, kSiteKFull)) { alive = false; break; }
         if (!wait_turn()) { alive = false; break; }
         tc_fence_after();
-        if (lane == 0) issue_s(base);
+        if (lane == 0) {
+          issue_s(base, 0, D / 16);
+          commit_s(base);
+        }
         __syncwarp();
         pass_turn();
         for (int j = 0; j < n; ++j) {
@@ -441,12 +454,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++p_it;
           if (!wait_turn()) { alive = false; break; }
           tc_fence_after();
+          // An MMA issue returns only once the tensor core has taken the
+          // instruction, near the end of the work queued before it.  The turn
+          // goes to the other issuer while the last kTurnEarly MMAs of this
+          // bracket are still to be issued: they are queued well before the
+          // other issuer wakes up, so its bracket follows without a gap.
           if (lane == 0) {
-            issue_pv(idx, j > 0);
-            if (more) issue_s(idx + 1);
+            if (more) {
+              issue_pv(idx, j > 0, 0, 8);
+              commit_pv(idx);
+              issue_s(idx + 1, 0, D / 16 - kTurnEarly);
+            } else {
+              issue_pv(idx, j > 0, 0, 8 - kTurnEarly);
+            }
           }
           __syncwarp();
           pass_turn();
+          if (lane == 0) {
+            if (more) {
+              issue_s(idx + 1, D / 16 - kTurnEarly, D / 16);
+              commit_s(idx + 1);
+            } else {
+              issue_pv(idx, j > 0, 8 - kTurnEarly, 8);
+              commit_pv(idx);
+            }
+          }
+          __syncwarp();
         }
         kv_it = base + n;
         if (!alive) break;
