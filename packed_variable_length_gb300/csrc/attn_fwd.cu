@@ -29,16 +29,20 @@
 //               tensor core works on one query tile while the other tile's
 //               softmax runs, and each issuer checks its gates while the
 //               other one issues.  PV reads P straight from TMEM.
-//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: thread t owns
-//               query row t (TMEM lane t).  The whole 128-key row of S comes
-//               into registers with one TMEM wait (warpgroup 2 gives up
-//               registers for this); in PARTIAL tiles inadmissible keys are
-//               set to -inf.  Then the row max, P = exp2(scale*log2e*S - m)
-//               with its row sum, and P written as packed bf16 over the first
-//               64 columns of the same S buffer.  O is rescaled in TMEM only when the
-//               running max grows by more than 2^8 (the stale max bounds
-//               every P by 256 and the final division uses the same max).
-//               The epilogue divides by the row sum and writes O and LSE.
+//   warps 0-7   softmax, tile A then tile B of each key tile: warp w holds
+//               query rows 32 (w % 4) .. + 31 (its TMEM lanes) and key half
+//               w / 4 of them, so that the two warps on each SM
+//               sub-partition share its exponential unit.  A half row of S
+//               comes into registers with one TMEM wait (warpgroup 2 gives
+//               up registers for this); in PARTIAL tiles inadmissible keys
+//               are set to -inf.  The two halves swap their partial row
+//               maxima (shared memory and an mbarrier per warp pair), then
+//               P = exp2(scale*log2e*S - m) with its row sum, and P written
+//               as packed bf16 over the first 64 columns of the same S
+//               buffer.  O is rescaled in TMEM only when the running max
+//               grows by more than 2^8 (the stale max bounds every P by 256
+//               and the final division uses the same max).  The epilogue
+//               adds the halves' row sums, divides and writes O and LSE.
 // Every wait is bounded; on expiry the CTA records the failure, drains its
 // outstanding copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -49,8 +53,9 @@
 namespace pvl {
 namespace {
 
-// warps 0-7 softmax (two warpgroups), 8 TMA, 9 and 10 MMA issuers (tiles A
-// and B), 11 idle; warpgroup 2's registers go to the softmax groups
+// warps 0-7 softmax (two warpgroups, one per key half), 8 TMA, 9 and 10 MMA
+// issuers (tiles A and B), 11 idle; warpgroup 2's registers go to the
+// softmax groups
 constexpr int kThreads = 384;
 // registers per thread after reallocation: 256 x 208 + 128 x 88 = 384 x 168,
 // the launch's own allotment (168 = 65536 / 384 rounded down to 8)
@@ -61,7 +66,7 @@ constexpr int kMmaWarp = 9;    // MMA issuer of query tile A; owns TMEM
 constexpr int kMmaWarpB = 10;  // MMA issuer of query tile B
 constexpr int kStages = 2;
 // MMAs of a bracket issued after the turn has passed to the other issuer
-constexpr int kTurnEarly = 2;
+constexpr int kTurnEarly = 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S_X at [128 X, 128 X + 128); P_X packed over its first 64 columns
 constexpr uint32_t kColO = 256;  // O_X at [256 + X D, 256 + (X + 1) D)
@@ -69,7 +74,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum FwdSite : uint32_t {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull, kSitePFull, kSiteOFree,
-  kSiteSFull, kSitePvDone, kSiteTurn, kSiteItemEmpty, kSiteItemFull
+  kSiteSFull, kSitePvDone, kSiteTurn, kSiteItemEmpty, kSiteItemFull, kSiteXch
 };
 
 // Work items are handed out at run time: the producer thread takes the next
@@ -152,30 +157,31 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// One query row of S (128 keys) into registers with a single TMEM wait; in a
-// PARTIAL tile the inadmissible keys are set to -inf, so that they drop out
-// of the max and exponentiate to 0.  Returns the row max of S.
+// Half hf of one query row of S (keys [64 hf, 64 hf + 64)) into registers
+// with a single TMEM wait; in a PARTIAL tile the inadmissible keys are set to
+// -inf, so that they drop out of the max and exponentiate to 0.  Returns the
+// max over these 64 keys.
 template <bool kMasked>
-__device__ __forceinline__ float load_row(uint32_t s_col, uint32_t (&s)[4][32], const int32_t* seq_row, int L, int kt,
-                                          int my_seq) {
+__device__ __forceinline__ float load_half_row(uint32_t s_col, int hf, uint32_t (&s)[2][32], const int32_t* seq_row,
+                                               int L, int kt, int my_seq) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) tmem_ld32(s_col + 32 * c, s[c]);
-  uint32_t mk[4];
+  for (int c = 0; c < 2; ++c) tmem_ld32(s_col + 64 * hf + 32 * c, s[c]);
+  uint32_t mk[2];
   if (kMasked) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) mk[c] = key_mask_word(seq_row, L, kt, c, my_seq);
+    for (int c = 0; c < 2; ++c) mk[c] = key_mask_word(seq_row, L, kt, 2 * hf + c, my_seq);
   }
   tmem_wait_ld();
   if (kMasked) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         if (!((mk[c] >> i) & 1u)) s[c][i] = __float_as_uint(-INFINITY);
   }
   float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
+  for (int c = 0; c < 2; ++c)
 #pragma unroll
     for (int i = 0; i < 32; i += 8)
 #pragma unroll
@@ -184,15 +190,17 @@ __device__ __forceinline__ float load_row(uint32_t s_col, uint32_t (&s)[4][32], 
   return fmax3(m[0], m[1], fmaxf(m[2], m[3]));
 }
 
-// P = 2^(scale_log2 * S + neg_m) for one row held in registers, written as
-// packed bf16 over the first 64 columns of the same S buffer; returns the row
-// sum of P.  Masked keys hold -inf and give exactly 0.
-__device__ __forceinline__ float exp_store(uint32_t s_col, const uint32_t (&s)[4][32], float scale_log2, float neg_m) {
+// P = 2^(scale_log2 * S + neg_m) for half hf of one row held in registers,
+// written as packed bf16 over columns [32 hf, 32 hf + 32) of the same S
+// buffer (P of keys 2c and 2c + 1 in column c); returns the sum of these 64
+// values of P.  Masked keys hold -inf and give exactly 0.
+__device__ __forceinline__ float exp_store_half(uint32_t s_col, int hf, const uint32_t (&s)[2][32], float scale_log2,
+                                                float neg_m) {
   const float2 c2 = make_float2(scale_log2, scale_log2);
   const float2 m2 = make_float2(neg_m, neg_m);
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < 2; ++c) {
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
@@ -202,7 +210,7 @@ __device__ __forceinline__ float exp_store(uint32_t s_col, const uint32_t (&s)[4
       else acc0 = fadd2(acc0, make_float2(p0, p1));
       pk[e >> 1] = pack_bf16x2(p0, p1);
     }
-    tmem_st16(s_col + 16 * c, pk);
+    tmem_st16(s_col + 32 * hf + 16 * c, pk);
   }
   return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
@@ -217,6 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_o_free[2], bar_final[2], bar_turn[2];
   __shared__ uint64_t bar_k_full[kStages], bar_k_empty[kStages], bar_v_full[kStages], bar_v_empty[kStages];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2];
+  // the two warps holding halves of the same 32 rows swap their partial row
+  // maxima (per key tile) and row sums (per item) here: [tile][slot][half][row]
+  __shared__ uint64_t bar_xch[2][4];
+  __shared__ float xch_s[2][2][2][128];
   __shared__ int item_s[kItemSlots];
   __shared__ uint64_t bar_item_full[kItemSlots], bar_item_empty[kItemSlots];
   __shared__ uint32_t tmem_base_s;
@@ -248,11 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_v_empty[s], 2);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&bar_o_free[x], 128);
+      mbar_init(&bar_o_free[x], 256);  // every softmax thread
       mbar_init(&bar_final[x], 1);
       mbar_init(&bar_turn[x], 1);
       mbar_init(&bar_s_full[x], 1);
-      mbar_init(&bar_p_full[x], 128);
+      mbar_init(&bar_p_full[x], 256);
+      for (int q = 0; q < 4; ++q) mbar_init(&bar_xch[x][q], 2);  // lane 0 of each warp of the pair
       mbar_init(&bar_pv_done[x], 1);
     }
     for (int s = 0; s < kItemSlots; ++s) {
@@ -496,16 +509,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------- softmax
+    // Both warpgroups work on each query tile, tile A then tile B of each key
+    // tile: warp w holds rows 32 (w % 4) .. + 31 (its TMEM lanes) and key
+    // half hf = w / 4 of them, so that two warps share each SM sub-partition
+    // and one's FMA work fills the other's waits for the exponential unit.
+    // The two warps of a pair swap partial row maxima through shared memory
+    // (an mbarrier pair wait, bounded) and agree on the running max.
     regs_inc<kRegsSoftmax>();
-    const int x = warp >> 2;            // query tile of the pair: 0 = A, 1 = B
-    const int row = threadIdx.x & 127;  // query row inside the tile == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_col = tmem + lane_base + kColS + x * 128;
-    const uint32_t o_col = tmem + lane_base + kColO + x * D;
+    const int hf = warp >> 2;            // key half: columns [64 hf, 64 hf + 64) of S
+    const int q4 = warp & 3;             // lane quarter
+    const int row = threadIdx.x & 127;   // query row inside the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    constexpr int kHalfD = D / 2;        // O columns of this half
     uint32_t s_it = 0, pv_it = 0;
+    uint32_t xc_it[2] = {0u, 0u};        // exchanges per tile
     bool alive = true;
     auto waitw = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
+    };
+    // publish v for the partner warp and return the partner's value
+    auto swap = [&](int x, float v, float& other) {
+      const uint32_t slot = xc_it[x] & 1;
+      xch_s[x][slot][hf][row] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_xch[x][q4]);
+      if (!waitw(&bar_xch[x][q4], slot, kSiteXch)) return false;
+      other = xch_s[x][slot][hf ^ 1][row];
+      ++xc_it[x];
+      return true;
     };
     for (uint32_t it = 0; alive; ++it) {
       const int slot = it % kItemSlots;
@@ -518,96 +549,126 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = static_cast<int>(w / p.n_pairs);
       const int b = tile / nP, pp = tile % nP;
       const int n = p.row_count[tile];
-      const int qpos = pp * 256 + x * 128 + row;
-      const bool in_range = qpos < p.Lq;
-      __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Lq + qpos) * p.H + h) * D;
-      float* lse_out = p.lse + (static_cast<size_t>(b) * p.H + h) * p.Lq + qpos;
       if (n == 0) {  // no valid query in this pair of tiles
-        if (in_range) {
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
-          *lse_out = -INFINITY;
+        for (int x = 0; x < 2; ++x) {
+          const int qpos = pp * 256 + x * 128 + row;
+          if (qpos < p.Lq) {
+            __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Lq + qpos) * p.H + h) * D + hf * kHalfD;
+#pragma unroll
+            for (int c = 0; c < kHalfD / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+            if (hf == 0) p.lse[(static_cast<size_t>(b) * p.H + h) * p.Lq + qpos] = -INFINITY;
+          }
         }
         continue;
       }
       const int nfull = p.row_full[tile];
       const int32_t* list = p.row_list + static_cast<size_t>(tile) * nK;
       const int32_t* seq_row = p.k_seq + static_cast<size_t>(b) * p.Lk;  // key ids of this row
-      const int my_seq = in_range ? p.q_seq[static_cast<size_t>(b) * p.Lq + qpos] : -1;
-      float m_ref = -INFINITY;  // running max of scale*log2(e)*s
-      float l = 0.0f;           // running sum of 2^(...) relative to m_ref
-      for (int j = 0; j < n; ++j) {
+      int my_seq[2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int qpos = pp * 256 + x * 128 + row;
+        my_seq[x] = qpos < p.Lq ? p.q_seq[static_cast<size_t>(b) * p.Lq + qpos] : -1;
+      }
+      float m_ref[2] = {-INFINITY, -INFINITY};  // running max of scale*log2(e)*s, per tile
+      float l[2] = {0.0f, 0.0f};                // this half's running sum of 2^(...) relative to m_ref
+      for (int j = 0; j < n && alive; ++j) {
         const bool partial = j >= nfull;
         const int kt = partial ? list[j] : 0;
-        if (!waitw(&bar_s_full[x], s_it & 1, kSiteSFull)) { alive = false; break; }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const uint32_t s_col = tmem + lane_base + kColS + x * 128;
+          if (!waitw(&bar_s_full[x], s_it & 1, kSiteSFull)) { alive = false; break; }
+          tc_fence_after();
+          // this half of the S row into registers (PARTIAL tiles: inadmissible keys -> -inf)
+          uint32_t srow[2][32];
+          float mh;
+          if (!partial) mh = load_half_row<false>(s_col, hf, srow, seq_row, p.Lk, kt, my_seq[x]);
+          else mh = load_half_row<true>(s_col, hf, srow, seq_row, p.Lk, kt, my_seq[x]);
+          // the partner has loaded its half too once the swap completes, so
+          // P may then be written over S columns [0, 64)
+          float mo;
+          if (!swap(x, mh, mo)) { alive = false; break; }
+          const float mx2 = fmaxf(mh, mo) * p.scale_log2;
+          const bool grow = mx2 > m_ref[x] + kRescaleThreshold;
+          const float m_new = grow ? mx2 : m_ref[x];
+          const float alpha = grow ? ex2(m_ref[x] - m_new) : 1.0f;
+          const bool any = m_new != -INFINITY;
+          const float neg_m = any ? -m_new : 0.0f;
+          // P = 2^(scale*log2e*S - m), packed bf16 over S columns [32 hf, 32 hf + 32)
+          const float lsum = exp_store_half(s_col, hf, srow, p.scale_log2, neg_m);
+          l[x] = l[x] * alpha + lsum;
+          // PV_x of the previous key tile has completed: S_x of this tile was
+          // issued after it by the same thread, and the commit that completed
+          // s_full tracks every earlier MMA of that thread, so its pv_done
+          // phase needs no wait of its own (only the item's last one is waited
+          // for, before the epilogue).  Rescale this half's O_x columns when
+          // the max grew.
+          if (j > 0) {
+            const bool rescale = grow && m_ref[x] != -INFINITY;
+            if (__any_sync(0xffffffffu, rescale)) {
+              const float f = rescale ? alpha : 1.0f;
+              const uint32_t o_col = tmem + lane_base + kColO + x * D + hf * kHalfD;
+#pragma unroll
+              for (int c = 0; c < kHalfD / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(o_col + c * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+                tmem_st32(o_col + c * 32, r);
+              }
+            }
+          }
+          m_ref[x] = m_new;
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bar_p_full[x]);
+        }
+        if (!alive) break;
         ++s_it;
+        if (j > 0) ++pv_it;
+      }
+      if (!alive) break;
+      // epilogues: the last PV_x has finished
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (!waitw(&bar_pv_done[x], pv_it & 1, kSitePvDone)) { alive = false; break; }
         tc_fence_after();
-        // S row into registers (PARTIAL tiles: inadmissible keys -> -inf)
-        uint32_t srow[4][32];
-        float mx;
-        if (!partial) mx = load_row<false>(s_col, srow, seq_row, p.Lk, kt, my_seq);
-        else mx = load_row<true>(s_col, srow, seq_row, p.Lk, kt, my_seq);
-        const float mx2 = mx * p.scale_log2;
-        const bool grow = mx2 > m_ref + kRescaleThreshold;
-        const float m_new = grow ? mx2 : m_ref;
-        const float alpha = grow ? ex2(m_ref - m_new) : 1.0f;
-        const bool any = m_new != -INFINITY;
-        const float neg_m = any ? -m_new : 0.0f;
-        // P = 2^(scale*log2e*S - m), packed bf16 over S columns [0, 64)
-        const float lsum = exp_store(s_col, srow, p.scale_log2, neg_m);
-        l = l * alpha + lsum;
-        // PV_x of the previous key tile has completed: S_x of this tile was
-        // issued after it by the same thread, and the commit that completed
-        // s_full tracks every earlier MMA of that thread, so its pv_done
-        // phase needs no wait of its own (only the item's last one is waited
-        // for, before the epilogue).  Rescale O_x when the max grew.
-        if (j > 0) {
-          ++pv_it;
-          const bool rescale = grow && m_ref != -INFINITY;
-          if (__any_sync(0xffffffffu, rescale)) {
-            const float f = rescale ? alpha : 1.0f;
+        float lo;
+        if (!swap(x, l[x], lo)) { alive = false; break; }
+        const float lt = l[x] + lo;
+        const float inv_l = lt > 0.0f ? 1.0f / lt : 0.0f;
+        const int qpos = pp * 256 + x * 128 + row;
+        const bool in_range = qpos < p.Lq;
+        __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Lq + qpos) * p.H + h) * D + hf * kHalfD;
+        const uint32_t o_col = tmem + lane_base + kColO + x * D + hf * kHalfD;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(o_col + c * 32, r);
-              tmem_wait_ld();
+        for (int c = 0; c < kHalfD / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_col + c * 32, r);
+          tmem_wait_ld();
+          if (in_range) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-              tmem_st32(o_col + c * 32, r);
+            for (int v = 0; v < 4; ++v) {
+              uint4 out;
+              out.x = pack_bf16x2(__uint_as_float(r[v * 8 + 0]) * inv_l, __uint_as_float(r[v * 8 + 1]) * inv_l);
+              out.y = pack_bf16x2(__uint_as_float(r[v * 8 + 2]) * inv_l, __uint_as_float(r[v * 8 + 3]) * inv_l);
+              out.z = pack_bf16x2(__uint_as_float(r[v * 8 + 4]) * inv_l, __uint_as_float(r[v * 8 + 5]) * inv_l);
+              out.w = pack_bf16x2(__uint_as_float(r[v * 8 + 6]) * inv_l, __uint_as_float(r[v * 8 + 7]) * inv_l);
+              reinterpret_cast<uint4*>(orow)[c * 4 + v] = out;
             }
           }
         }
-        m_ref = m_new;
-        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bar_p_full[x]);
+        mbar_arrive(&bar_o_free[x]);
+        if (in_range && hf == 0)
+          p.lse[(static_cast<size_t>(b) * p.H + h) * p.Lq + qpos] =
+              lt > 0.0f ? (m_ref[x] + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
       }
       if (!alive) break;
-      // epilogue: the last PV_x has finished
-      if (!waitw(&bar_pv_done[x], pv_it & 1, kSitePvDone)) { alive = false; break; }
       ++pv_it;
-      tc_fence_after();
-      const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(o_col + c * 32, r);
-        tmem_wait_ld();
-        if (in_range) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 out;
-            out.x = pack_bf16x2(__uint_as_float(r[v * 8 + 0]) * inv_l, __uint_as_float(r[v * 8 + 1]) * inv_l);
-            out.y = pack_bf16x2(__uint_as_float(r[v * 8 + 2]) * inv_l, __uint_as_float(r[v * 8 + 3]) * inv_l);
-            out.z = pack_bf16x2(__uint_as_float(r[v * 8 + 4]) * inv_l, __uint_as_float(r[v * 8 + 5]) * inv_l);
-            out.w = pack_bf16x2(__uint_as_float(r[v * 8 + 6]) * inv_l, __uint_as_float(r[v * 8 + 7]) * inv_l);
-            reinterpret_cast<uint4*>(orow)[c * 4 + v] = out;
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&bar_o_free[x]);
-      if (in_range) *lse_out = l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
 

@@ -67,7 +67,7 @@ def test_bounded_wait_times_out_and_the_context_survives(pvl):
     assert err < 2e-2
 
 
-FWD_SITES = range(1, 14)    # the forward kernel's wait sites
+FWD_SITES = range(1, 15)    # the forward kernel's wait sites
 BWD_SITES = range(21, 37)   # the main backward kernel's wait sites
 
 
