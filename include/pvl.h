@@ -21,7 +21,9 @@
  *    allocates no device memory at run time.  Its static device globals, held
  *    by every GPU that loads it until the process exits, are: a 16-byte error
  *    record, the PVL_NO_ALLOC_SCRATCH_BYTES scratch array of
- *    masked_attn_bwd_no_alloc, and two 32-bit result words of
+ *    masked_attn_bwd_no_alloc, 256 32-bit work-item counters of the forward
+ *    (one per (device, stream) in use; when all are taken the forward shares
+ *    its items out in fixed turns instead), and two 32-bit result words of
  *    pvl_selftest_wait_timeout.  Calls are asynchronous on `stream` (NULL =
  *    legacy default stream) and return after enqueueing.
  *  - Arguments are validated on the host before anything is launched; a
