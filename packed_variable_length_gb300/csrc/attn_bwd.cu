@@ -125,8 +125,12 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_base, int kk) {
 // ------------------------------------------------------------- preprocess
 // One group of D/8 lanes per (b, l, h) row: Delta = <dO, O> in fp32,
 // LSE * log2(e), the row's query seq_id (h = 0), and the row's dQ accumulator
-// set to zero.  Then the padding positions L <= l < Lp of the padded arrays.
-template <int D>
+// set to zero unless the query is padding (seq_id -1: its accumulator row
+// only ever receives zeros, and the conversion writes its dQ = 0 without
+// reading it).  Then the padding positions L <= l < Lp of the padded arrays.
+// Idx: the index type, 32-bit whenever B * L * H * D / 8 fits (the
+// divisions by H and L are then short).
+template <int D, typename Idx>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
                                                       const float* __restrict__ lse, const int32_t* __restrict__ seq_id,
@@ -136,16 +140,16 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   constexpr int G = D / 8;
   const int lane = threadIdx.x & 31;
   if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0u;  // the main kernel's work-item counter
-  const long long rows = static_cast<long long>(B) * L * H;
-  const long long total = rows * G;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;  // a multiple of 32
+  const Idx uH = static_cast<Idx>(H), uL = static_cast<Idx>(L);
+  const Idx rows = static_cast<Idx>(B) * uL * uH;
+  const Idx total = rows * G;
+  const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;  // a multiple of 32
   // warp-aligned loop: every lane of a warp runs the same iterations, so the
   // shuffles below always see the whole warp
-  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
-       base += stride) {
-    const long long t = base + lane;
+  for (Idx base = static_cast<Idx>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total; base += stride) {
+    const Idx t = base + lane;
     const bool act = t < total;
-    const long long row = act ? t / G : 0;
+    const Idx row = act ? t / G : 0;
     const int part = static_cast<int>(t % G);
     float s = 0.0f;
     if (act) {
@@ -164,22 +168,25 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 #pragma unroll
     for (int off = G / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (act) {
-      float4* acc = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
-      acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const Idx bl = row / uH;
+      if (seq_id[bl] >= 0) {
+        float4* acc = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * D + part * 8);
+        acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       if (part == 0) {
-        const long long bl = row / H;
-        const int h = static_cast<int>(row % H);
-        const long long b = bl / L;
-        const long long l = bl % L;
+        const size_t h = row - bl * uH;
+        const size_t b = bl / uL;
+        const size_t l = bl - b * uL;
         delta[(b * H + h) * Lp + l] = s;
         lse2[(b * H + h) * Lp + l] = lse[(b * H + h) * L + l] * 1.4426950408889634f;
-        if (h == 0) qseq[b * Lp + l] = seq_id[b * L + l];
+        if (h == 0) qseq[b * Lp + l] = seq_id[bl];
       }
     }
   }
   const long long pad = static_cast<long long>(B) * H * (Lp - L);
-  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < pad; t += stride) {
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < pad;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long bh = t / (Lp - L);
     const long long l = L + t % (Lp - L);
     delta[bh * Lp + l] = 0.0f;
@@ -189,11 +196,22 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 }
 
 // ------------------------------------------------------------------ convert
+// dQ = bf16(scale * accumulator) per group of 8 features; padding queries
+// (seq_id -1, whose accumulator rows were not zeroed) get exact zeros
+// without a read of the accumulator.
+template <typename Idx>
 __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restrict__ dq_acc,
-                                                          __nv_bfloat16* __restrict__ dq, float scale, long long n8) {
-  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = gid; i < n8; i += stride) {
+                                                          const int32_t* __restrict__ seq_id,
+                                                          __nv_bfloat16* __restrict__ dq, float scale, long long n8_,
+                                                          int groups_per_pos) {
+  const Idx n8 = static_cast<Idx>(n8_), gpp = static_cast<Idx>(groups_per_pos);
+  const Idx gid = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;
+  for (Idx i = gid; i < n8; i += stride) {
+    if (seq_id[i / gpp] < 0) {  // (b, l) of this group: H * D / 8 groups per position
+      reinterpret_cast<uint4*>(dq)[i] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
     const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
     const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
     uint4 out;
@@ -695,9 +713,16 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   unsigned int* sched = reinterpret_cast<unsigned int*>(wsb + bwd_ws_sched_offset(B, L, H, D));
   const long long rows = static_cast<long long>(B) * L * H;
 
-  bwd_pre_kernel<D><<<grid_for(rows * (D / 8), 256), 256, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), lse, q_seq, delta, lse2,
-      qseq, dq_acc, sched, B, L, Lp, H);
+  // 32-bit indices when every index (and its grid-stride successor) fits
+  const bool idx32 = rows * (D / 8) + static_cast<long long>(sms) * 8 * 256 < (1ll << 31);
+  if (idx32)
+    bwd_pre_kernel<D, uint32_t><<<grid_for(rows * (D / 8), 256), 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), lse, q_seq, delta,
+        lse2, qseq, dq_acc, sched, B, L, Lp, H);
+  else
+    bwd_pre_kernel<D, unsigned long long><<<grid_for(rows * (D / 8), 256), 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), lse, q_seq, delta,
+        lse2, qseq, dq_acc, sched, B, L, Lp, H);
   st = check_cuda(cudaGetLastError(), "masked_attn_bwd preprocess launch");
   if (st != PVL_OK) return st;
 
@@ -747,7 +772,12 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   }
 
   const long long n8 = rows * D / 8;
-  bwd_convert_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(dq_acc, reinterpret_cast<__nv_bfloat16*>(dq), scale, n8);
+  if (idx32)
+    bwd_convert_kernel<uint32_t><<<grid_for(n8, 256), 256, 0, stream>>>(
+        dq_acc, q_seq, reinterpret_cast<__nv_bfloat16*>(dq), scale, n8, H * D / 8);
+  else
+    bwd_convert_kernel<unsigned long long><<<grid_for(n8, 256), 256, 0, stream>>>(
+        dq_acc, q_seq, reinterpret_cast<__nv_bfloat16*>(dq), scale, n8, H * D / 8);
   return check_cuda(cudaGetLastError(), "masked_attn_bwd convert launch");
 }
 
