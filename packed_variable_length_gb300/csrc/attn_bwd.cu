@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const bool act = t < total;
     const Idx row = act ? t / G : 0;
     const int part = static_cast<int>(t % G);
+    const Idx bl = row / uH;
+    const int my_id = act ? seq_id[bl] : -1;  // issued with the row's loads
     float s = 0.0f;
     if (act) {
       const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[part];
@@ -168,8 +170,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 #pragma unroll
     for (int off = G / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (act) {
-      const Idx bl = row / uH;
-      if (seq_id[bl] >= 0) {
+      if (my_id >= 0) {
         float4* acc = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * D + part * 8);
         acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
         acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
         const size_t l = bl - b * uL;
         delta[(b * H + h) * Lp + l] = s;
         lse2[(b * H + h) * Lp + l] = lse[(b * H + h) * L + l] * 1.4426950408889634f;
-        if (h == 0) qseq[b * Lp + l] = seq_id[bl];
+        if (h == 0) qseq[b * Lp + l] = my_id;
       }
     }
   }
