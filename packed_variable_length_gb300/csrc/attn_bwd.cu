@@ -128,6 +128,9 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_base, int kk) {
 // set to zero unless the query is padding (seq_id -1: its accumulator row
 // only ever receives zeros, and the conversion writes its dQ = 0 without
 // reading it).  Then the padding positions L <= l < Lp of the padded arrays.
+// Row groups per thread and loop iteration of the preprocess (their loads
+// issued together; four measured no faster than two).
+constexpr int kPreUnroll = 2;
 // Idx: the index type, 32-bit whenever B * L * H * D / 8 fits (the
 // divisions by H and L are then short).
 template <int D, typename Idx>
@@ -145,43 +148,57 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   const Idx total = rows * G;
   const Idx stride = static_cast<Idx>(gridDim.x) * blockDim.x;  // a multiple of 32
   // warp-aligned loop: every lane of a warp runs the same iterations, so the
-  // shuffles below always see the whole warp
-  for (Idx base = static_cast<Idx>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total; base += stride) {
-    const Idx t = base + lane;
-    const bool act = t < total;
-    const Idx row = act ? t / G : 0;
-    const int part = static_cast<int>(t % G);
-    const Idx bl = row / uH;
-    const int my_id = act ? seq_id[bl] : -1;  // issued with the row's loads
-    float s = 0.0f;
-    if (act) {
-      const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[part];
-      const uint4 c = reinterpret_cast<const uint4*>(dO + row * D)[part];
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+  // shuffles below always see the whole warp.  kPreUnroll groups of rows per
+  // iteration, their loads issued together (more bytes in flight per thread).
+  for (Idx base = static_cast<Idx>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
+       base += kPreUnroll * stride) {
+    Idx t[kPreUnroll], row[kPreUnroll], bl[kPreUnroll];
+    bool act[kPreUnroll];
+    int part[kPreUnroll], my_id[kPreUnroll];
+    uint4 a[kPreUnroll], c[kPreUnroll];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 x = __bfloat1622float2(a2[i]);
-        const float2 y = __bfloat1622float2(c2[i]);
-        s = fmaf(x.x, y.x, s);
-        s = fmaf(x.y, y.y, s);
+    for (int u = 0; u < kPreUnroll; ++u) {
+      t[u] = base + u * stride + lane;
+      act[u] = t[u] < total;
+      row[u] = act[u] ? t[u] / G : 0;
+      part[u] = static_cast<int>(t[u] % G);
+      bl[u] = row[u] / uH;
+      my_id[u] = act[u] ? seq_id[bl[u]] : -1;
+      if (act[u]) {
+        a[u] = reinterpret_cast<const uint4*>(o + static_cast<size_t>(row[u]) * D)[part[u]];
+        c[u] = reinterpret_cast<const uint4*>(dO + static_cast<size_t>(row[u]) * D)[part[u]];
       }
     }
 #pragma unroll
-    for (int off = G / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (act) {
-      if (my_id >= 0) {
-        float4* acc = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * D + part * 8);
-        acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < kPreUnroll; ++u) {
+      float s = 0.0f;
+      if (act[u]) {
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+        const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c[u]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 x = __bfloat1622float2(a2[i]);
+          const float2 y = __bfloat1622float2(c2[i]);
+          s = fmaf(x.x, y.x, s);
+          s = fmaf(x.y, y.y, s);
+        }
       }
-      if (part == 0) {
-        const size_t h = row - bl * uH;
-        const size_t b = bl / uL;
-        const size_t l = bl - b * uL;
-        delta[(b * H + h) * Lp + l] = s;
-        lse2[(b * H + h) * Lp + l] = lse[(b * H + h) * L + l] * 1.4426950408889634f;
-        if (h == 0) qseq[b * Lp + l] = my_id;
+#pragma unroll
+      for (int off = G / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (act[u]) {
+        if (my_id[u] >= 0) {
+          float4* acc = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row[u]) * D + part[u] * 8);
+          acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+          acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (part[u] == 0) {
+          const size_t h = row[u] - bl[u] * uH;
+          const size_t b = bl[u] / uL;
+          const size_t l = bl[u] - b * uL;
+          delta[(b * H + h) * Lp + l] = s;
+          lse2[(b * H + h) * Lp + l] = lse[(b * H + h) * L + l] * 1.4426950408889634f;
+          if (h == 0) qseq[b * Lp + l] = my_id[u];
+        }
       }
     }
   }
@@ -715,7 +732,7 @@ pvl_status launch_bwd(const pvl_bf16* q, const pvl_bf16* k, const pvl_bf16* v, c
   const long long rows = static_cast<long long>(B) * L * H;
 
   // 32-bit indices when every index (and its grid-stride successor) fits
-  const bool idx32 = rows * (D / 8) + static_cast<long long>(sms) * 8 * 256 < (1ll << 31);
+  const bool idx32 = rows * (D / 8) + static_cast<long long>(kPreUnroll) * sms * 8 * 256 < (1ll << 31);
   if (idx32)
     bwd_pre_kernel<D, uint32_t><<<grid_for(rows * (D / 8), 256), 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), lse, q_seq, delta,
