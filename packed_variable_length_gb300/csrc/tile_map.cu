@@ -9,7 +9,9 @@
 //   2. tile_lists:  one warp per query tile (and per key tile) classifies its
 //                   pairs from the stats and compacts FULL then PARTIAL
 //                   indices with ballots;
-//   3. tile_order:  bitonic sort in shared memory of (count desc, index asc).
+//   3. tile_order:  bitonic sort of (count desc, index asc): in registers with
+//                   warp shuffles for partners less than 32 apart when every
+//                   thread holds one key, else in shared memory.
 #include <cuda_runtime.h>
 
 #include "pvl_internal.h"
@@ -120,6 +122,7 @@ __device__ __forceinline__ uint8_t classify(int nvq, int loq, int hiq, int bm, i
 }
 
 constexpr int kListWarps = 8;
+constexpr int kGroup = 8;  // chunks of 32 classified per load round
 
 // One warp per list.  Warps [0, B*nTq) own query tile rows (and write CLS),
 // warps [B*nTq, B*nTq + B*nTk) own key tile columns.
@@ -140,23 +143,41 @@ __global__ void __launch_bounds__(kListWarps * 32) tile_lists_kernel(int B, int 
   const int hi0 = is_row ? m.q_hi[b * nTq + t] : m.k_hi[b * nTk + t];
   int32_t* list = is_row ? m.row_list + (static_cast<size_t>(b) * nTq + t) * nTk
                          : m.col_list + (static_cast<size_t>(b) * nTk + t) * nTq;
+  // the other side's summaries of this batch row
+  const int32_t* o_nv = is_row ? m.k_nv + b * nTk : m.q_nv + b * nTq;
+  const int32_t* o_lo = is_row ? m.k_lo + b * nTk : m.q_lo + b * nTq;
+  const int32_t* o_hi = is_row ? m.k_hi + b * nTk : m.q_hi + b * nTq;
   int written = 0, nfull = 0;
   for (int pass = 0; pass < 2; ++pass) {
     const uint8_t want = pass == 0 ? kFull : kPartial;
-    for (int base = 0; base < n_other; base += 32) {
-      const int o = base + lane;
-      uint8_t c = kEmpty;
-      if (o < n_other) {
-        if (is_row) {
-          c = classify(nv0, lo0, hi0, bm, m.k_nv[b * nTk + o], m.k_lo[b * nTk + o], m.k_hi[b * nTk + o], bn);
-          if (pass == 0) m.cls[(static_cast<size_t>(b) * nTq + t) * nTk + o] = c;
-        } else {
-          c = classify(m.q_nv[b * nTq + o], m.q_lo[b * nTq + o], m.q_hi[b * nTq + o], bm, nv0, lo0, hi0, bn);
+    // kGroup chunks of 32 per step: their loads are issued together, so the
+    // list pays one load latency per group instead of one per chunk
+    for (int base0 = 0; base0 < n_other; base0 += 32 * kGroup) {
+      int nv[kGroup], lo[kGroup], hi[kGroup];
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        const int o = base0 + 32 * u + lane;
+        nv[u] = 0;
+        lo[u] = hi[u] = 0;
+        if (o < n_other) {
+          nv[u] = __ldg(o_nv + o);
+          lo[u] = __ldg(o_lo + o);
+          hi[u] = __ldg(o_hi + o);
         }
       }
-      const unsigned hit = __ballot_sync(0xffffffffu, o < n_other && c == want);
-      if (c == want && o < n_other) list[written + __popc(hit & ((1u << lane) - 1u))] = o;
-      written += __popc(hit);
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        const int o = base0 + 32 * u + lane;
+        uint8_t c = kEmpty;
+        if (o < n_other) {
+          c = is_row ? classify(nv0, lo0, hi0, bm, nv[u], lo[u], hi[u], bn)
+                     : classify(nv[u], lo[u], hi[u], bm, nv0, lo0, hi0, bn);
+          if (is_row && pass == 0) m.cls[(static_cast<size_t>(b) * nTq + t) * nTk + o] = c;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, o < n_other && c == want);
+        if (c == want && o < n_other) list[written + __popc(hit & ((1u << lane) - 1u))] = o;
+        written += __popc(hit);
+      }
     }
     if (pass == 0) nfull = written;
   }
@@ -186,6 +207,32 @@ __global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(int nq, int n
   const int np2 = is_q ? npow2_q : npow2_k;
   const int32_t* cnt = is_q ? m.row_count : m.col_count;
   int32_t* out = is_q ? m.q_order : m.k_order;
+  if (np2 <= kOrderThreads) {
+    // one key per thread: partners less than 32 apart are in the same warp
+    // (shuffles); only the wider stages go through shared memory
+    const int i = threadIdx.x;
+    uint32_t key = i < n ? (static_cast<uint32_t>(PVL_MAX_ORDER_TILES - cnt[i]) << kIdxBits) | static_cast<uint32_t>(i)
+                         : 0xFFFFFFFFu;
+    for (int k = 2; k <= np2; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        uint32_t other;
+        if (j >= 32) {
+          if (i < np2) keys[i] = key;
+          __syncthreads();
+          other = i < np2 ? keys[i ^ j] : 0xFFFFFFFFu;
+          __syncthreads();
+        } else {
+          other = __shfl_xor_sync(0xffffffffu, key, j);
+        }
+        // the pair's lower index keeps the smaller key where the run ascends
+        const bool ascending = (i & k) == 0;
+        const bool lower = (i & j) == 0;
+        key = (lower == ascending) ? min(key, other) : max(key, other);
+      }
+    }
+    if (i < n) out[i] = static_cast<int32_t>(key & ((1u << kIdxBits) - 1u));
+    return;
+  }
   for (int i = threadIdx.x; i < np2; i += kOrderThreads)
     keys[i] = i < n ? (static_cast<uint32_t>(PVL_MAX_ORDER_TILES - cnt[i]) << kIdxBits) | static_cast<uint32_t>(i)
                     : 0xFFFFFFFFu;
