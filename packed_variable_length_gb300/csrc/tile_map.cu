@@ -3,8 +3,9 @@
 // per-tile work lists plus a longest-first order of the tiles.
 //
 // "lingbot_va_packing" §2.1-§2.2: FlexAttention derives a block mask from the
-// seq_ids and skips blocks with no admissible pair.  Here the map is built by
-// three small kernels on the caller's stream:
+// seq_ids and skips blocks with no admissible pair.  Here the map (both of
+// its levels at once) is built by three small kernels on the caller's
+// stream:
 //   1. tile_stats:  per tile, count / min / max of the valid ids;
 //   2. tile_lists:  one warp per query tile (and per key tile) classifies its
 //                   pairs from the stats and compacts FULL then PARTIAL
@@ -13,6 +14,8 @@
 //                   warp shuffles for partners less than 32 apart when every
 //                   thread holds one key, else in shared memory.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "pvl_internal.h"
 
@@ -51,16 +54,32 @@ TileMapPtrs tile_map_ptrs(void* ws, const TileMapLayout& t) {
 
 constexpr int kStatThreads = 128;
 
-// grid (nTq + nTk, B): blocks [0, nTq) summarise query tiles of block_m
-// positions over the query ids, the rest key tiles of block_n positions over
-// the key ids (the same array for self attention).
+// One level of the map: its arrays, tile sizes and tile counts.
+struct TileLevel {
+  TileMapPtrs m;
+  int bm, nTq, nTk;
+};
+struct TileLevels {
+  TileLevel lv[PVL_TM_LEVELS];
+};
+
+// grid (sum over levels of nTq + nTk, B), levels one after the other: in a
+// level's range, blocks [0, nTq) summarise query tiles of bm positions over
+// the query ids, the rest key tiles of bn positions over the key ids (the
+// same array for self attention).
 __global__ void __launch_bounds__(kStatThreads) tile_stats_kernel(const int32_t* __restrict__ q_seq,
                                                                   const int32_t* __restrict__ k_seq, int B, int Lq,
-                                                                  int Lk, int bm, int bn, int nTq, int nTk,
-                                                                  TileMapPtrs m) {
+                                                                  int Lk, int bn, TileLevels levels) {
+  int x = blockIdx.x, lvi = 0;
+  while (lvi + 1 < PVL_TM_LEVELS && x >= levels.lv[lvi].nTq + levels.lv[lvi].nTk) {
+    x -= levels.lv[lvi].nTq + levels.lv[lvi].nTk;
+    ++lvi;
+  }
+  const TileMapPtrs& m = levels.lv[lvi].m;
+  const int bm = levels.lv[lvi].bm, nTq = levels.lv[lvi].nTq, nTk = levels.lv[lvi].nTk;
   const int b = blockIdx.y;
-  const bool is_q = blockIdx.x < nTq;
-  const int t = is_q ? blockIdx.x : blockIdx.x - nTq;
+  const bool is_q = x < nTq;
+  const int t = is_q ? x : x - nTq;
   const int bs = is_q ? bm : bn;
   const int L = is_q ? Lq : Lk;
   const int32_t* seq_id = is_q ? q_seq : k_seq;
@@ -100,7 +119,7 @@ __global__ void __launch_bounds__(kStatThreads) tile_stats_kernel(const int32_t*
     (is_q ? m.q_nv : m.k_nv)[idx] = cnt;
     (is_q ? m.q_lo : m.k_lo)[idx] = lo;
     (is_q ? m.q_hi : m.k_hi)[idx] = hi;
-    if (blockIdx.x == 0 && b == 0) {
+    if (x == 0 && b == 0) {
       m.header[0] = kTileMapMagic;
       m.header[1] = kTileMapVersion;
       m.header[2] = B;
@@ -124,12 +143,20 @@ __device__ __forceinline__ uint8_t classify(int nvq, int loq, int hiq, int bm, i
 constexpr int kListWarps = 8;
 constexpr int kGroup = 8;  // chunks of 32 classified per load round
 
-// One warp per list.  Warps [0, B*nTq) own query tile rows (and write CLS),
-// warps [B*nTq, B*nTq + B*nTk) own key tile columns.
-__global__ void __launch_bounds__(kListWarps * 32) tile_lists_kernel(int B, int bm, int bn, int nTq, int nTk,
-                                                                     TileMapPtrs m) {
-  const long long w = static_cast<long long>(blockIdx.x) * kListWarps + (threadIdx.x >> 5);
+// One warp per list, levels one after the other.  In a level's range, warps
+// [0, B*nTq) own query tile rows (and write CLS), warps [B*nTq, B*nTq + B*nTk)
+// own key tile columns.
+__global__ void __launch_bounds__(kListWarps * 32) tile_lists_kernel(int B, int bn, TileLevels levels) {
+  long long w = static_cast<long long>(blockIdx.x) * kListWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  int lvi = 0;
+  while (lvi + 1 < PVL_TM_LEVELS &&
+         w >= static_cast<long long>(B) * (levels.lv[lvi].nTq + levels.lv[lvi].nTk)) {
+    w -= static_cast<long long>(B) * (levels.lv[lvi].nTq + levels.lv[lvi].nTk);
+    ++lvi;
+  }
+  const TileMapPtrs& m = levels.lv[lvi].m;
+  const int bm = levels.lv[lvi].bm, nTq = levels.lv[lvi].nTq, nTk = levels.lv[lvi].nTk;
   const long long nrows = static_cast<long long>(B) * nTq;
   const long long ncols = static_cast<long long>(B) * nTk;
   if (w >= nrows + ncols) return;
@@ -196,15 +223,17 @@ __global__ void __launch_bounds__(kListWarps * 32) tile_lists_kernel(int B, int 
 constexpr int kOrderThreads = 1024;
 constexpr int kIdxBits = 14;  // PVL_MAX_ORDER_TILES == 1 << 14
 
-// Block 0 sorts the query tiles, block 1 the key tiles.  Key =
-// (PVL_MAX_ORDER_TILES - count) << 14 | index, ascending, so larger counts come
-// first and ties keep ascending index; padding keys are 0xFFFFFFFF.
-__global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(int nq, int nk, int npow2_q, int npow2_k,
-                                                                   TileMapPtrs m) {
+// Two blocks per level: block 2 lv sorts the level's query tiles, block
+// 2 lv + 1 its key tiles.  Key = (PVL_MAX_ORDER_TILES - count) << 14 | index,
+// ascending, so larger counts come first and ties keep ascending index;
+// padding keys are 0xFFFFFFFF.
+__global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(int B, TileLevels levels) {
   extern __shared__ uint32_t keys[];
-  const bool is_q = blockIdx.x == 0;
-  const int n = is_q ? nq : nk;
-  const int np2 = is_q ? npow2_q : npow2_k;
+  const TileMapPtrs& m = levels.lv[blockIdx.x >> 1].m;
+  const bool is_q = (blockIdx.x & 1) == 0;
+  const int n = B * (is_q ? levels.lv[blockIdx.x >> 1].nTq : levels.lv[blockIdx.x >> 1].nTk);
+  int np2 = 1;
+  while (np2 < n) np2 <<= 1;
   const int32_t* cnt = is_q ? m.row_count : m.col_count;
   int32_t* out = is_q ? m.q_order : m.k_order;
   if (np2 <= kOrderThreads) {
@@ -288,34 +317,35 @@ pvl_status build_tile_map(const char* who, const int32_t* q_seq, const int32_t* 
   if (nq0 > PVL_MAX_ORDER_TILES || nk0 > PVL_MAX_ORDER_TILES)
     return fail(PVL_ERR_UNSUPPORTED, "%s: B * tiles = %lld exceeds %d", who, nq0 > nk0 ? nq0 : nk0,
                 PVL_MAX_ORDER_TILES);
+  TileLevels levels;
+  int stat_blocks = 0;
+  long long nwarps = 0, np2_max = 1;
   for (int lv = 0; lv < PVL_TM_LEVELS; ++lv) {
     const TileMapLayout& t = all.level[lv];
-    const int bm = lv == 0 ? block_m : 2 * block_m;
-    const long long nq = static_cast<long long>(B) * t.nTq, nk = static_cast<long long>(B) * t.nTk;
-    const TileMapPtrs m = tile_map_ptrs(tile_ws, t);
-
-    tile_stats_kernel<<<dim3(t.nTq + t.nTk, B), kStatThreads, 0, s>>>(q_seq, k_seq, B, Lq, Lk, bm, block_n, t.nTq,
-                                                                     t.nTk, m);
-    pvl_status st = check_cuda(cudaGetLastError(), "tile_stats launch");
-    if (st != PVL_OK) return st;
-
-    const long long nwarps = nq + nk;
-    tile_lists_kernel<<<static_cast<unsigned>((nwarps + kListWarps - 1) / kListWarps), kListWarps * 32, 0, s>>>(
-        B, bm, block_n, t.nTq, t.nTk, m);
-    st = check_cuda(cudaGetLastError(), "tile_lists launch");
-    if (st != PVL_OK) return st;
-
-    const int pq = next_pow2(static_cast<int>(nq)), pk = next_pow2(static_cast<int>(nk));
-    const int smem = (pq > pk ? pq : pk) * static_cast<int>(sizeof(uint32_t));
-    if (smem > 48 * 1024) {
-      st = check_cuda(cudaFuncSetAttribute(tile_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
-                      "tile_order smem attribute");
-      if (st != PVL_OK) return st;
-    }
-    tile_order_kernel<<<2, kOrderThreads, smem, s>>>(static_cast<int>(nq), static_cast<int>(nk), pq, pk, m);
-    st = check_cuda(cudaGetLastError(), "tile_order launch");
+    levels.lv[lv].m = tile_map_ptrs(tile_ws, t);
+    levels.lv[lv].bm = lv == 0 ? block_m : 2 * block_m;
+    levels.lv[lv].nTq = t.nTq;
+    levels.lv[lv].nTk = t.nTk;
+    stat_blocks += t.nTq + t.nTk;
+    nwarps += static_cast<long long>(B) * (t.nTq + t.nTk);
+    np2_max = std::max<long long>(np2_max, next_pow2(B * std::max(t.nTq, t.nTk)));
+  }
+  tile_stats_kernel<<<dim3(stat_blocks, B), kStatThreads, 0, s>>>(q_seq, k_seq, B, Lq, Lk, block_n, levels);
+  pvl_status st = check_cuda(cudaGetLastError(), "tile_stats launch");
+  if (st != PVL_OK) return st;
+  tile_lists_kernel<<<static_cast<unsigned>((nwarps + kListWarps - 1) / kListWarps), kListWarps * 32, 0, s>>>(
+      B, block_n, levels);
+  st = check_cuda(cudaGetLastError(), "tile_lists launch");
+  if (st != PVL_OK) return st;
+  const int smem = static_cast<int>(np2_max) * static_cast<int>(sizeof(uint32_t));
+  if (smem > 48 * 1024) {
+    st = check_cuda(cudaFuncSetAttribute(tile_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                    "tile_order smem attribute");
     if (st != PVL_OK) return st;
   }
+  tile_order_kernel<<<2 * PVL_TM_LEVELS, kOrderThreads, smem, s>>>(B, levels);
+  st = check_cuda(cudaGetLastError(), "tile_order launch");
+  if (st != PVL_OK) return st;
   return PVL_OK;
 }
 
