@@ -21,7 +21,7 @@ batches of 4 (160 episodes) in one step.
 
 `--workload cross_concat64k` (or cross_padded) measures cross attention
 instead: the same episodes as queries at 38 tokens per frame and as keys at 16
-tokens per frame, each side with its own seq_ids (12 launches per step: one
+tokens per frame, each side with its own seq_ids (9 launches per step: one
 seq_id build per side).
 
 Under torchrun (N > 1) every rank runs an independent replica of the step on
@@ -51,8 +51,8 @@ sys.path.insert(0, ROOT)
 METRIC = "effective masked-attn fwd+bwd TFLOP/s and tokens/s at 1 GB300; % of bf16 peak"
 FLOPS_PER_PAIR_FWD = 4
 FLOPS_PER_PAIR_BWD = 10
-# kernels per step: seq_ids 1, tile map 3 per level x 2 levels, forward 1, backward 3
-LAUNCHES_PER_STEP = 11
+# kernels per step: seq_ids 1, tile map 3 (both levels), forward 1, backward 3
+LAUNCHES_PER_STEP = 8
 
 
 def load_peaks():
@@ -1175,7 +1175,7 @@ def run_adaptive(args):
             times.append(time_step(layer_step(frames, fp), 3))
             tokens.append(T * sum(frames))
             loads.append(len(bt) * (T * fp) ** model.p)
-            n_launch += 11 * 4
+            n_launch += (LAUNCHES_PER_STEP + 3) * 4  # the attention step plus AdaLN forward (1) and backward (2)
         tps, step_t, idle = al.simulate_data_parallel(times, tokens, ADAPTIVE_RANKS)
         results[name] = {"batches": len(batches),
                          "compute_imbalance_rate_cv_modelled_load": round(al.coefficient_of_variation(loads), 4),
