@@ -28,7 +28,10 @@
 //               keeps the brackets in the order A, B, A, B, ..., so the
 //               tensor core works on one query tile while the other tile's
 //               softmax runs, and each issuer checks its gates while the
-//               other one issues.  PV reads P straight from TMEM.
+//               other one issues.  An issuer passes the turn before its
+//               bracket's last MMA and commits (an MMA issue returns only
+//               when the tensor core takes the instruction), so the other
+//               bracket queues right behind.  PV reads P straight from TMEM.
 //   warps 0-7   softmax, tile A then tile B of each key tile: warp w holds
 //               query rows 32 (w % 4) .. + 31 (its TMEM lanes) and key half
 //               w / 4 of them, so that the two warps on each SM
