@@ -957,7 +957,7 @@ def run_loss(args):
     loss = torch.empty(1, dtype=torch.float32, device="cuda")
     ws = torch.empty(pvl.masked_mse_ws_bytes(B, L, C), dtype=torch.uint8, device="cuda")
     flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")    # 256 MB > L2
-    sink = torch.empty(1, dtype=torch.float32, device="cuda")
+    sink = torch.empty((), dtype=torch.float32, device="cuda")
     bytes_step = 4 * n_valid * C + 2 * B * L * C + 4 * B * L + 4
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
@@ -1018,7 +1018,7 @@ def run_loss(args):
         "metric": "frame_valid-masked loss + gradient algorithmic GB/s at 1 GB300",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 in/out, fp32 arithmetic, fp64 cross-CTA sum", "data": "synthetic",
+        "dtype": "bf16 in/out, fp32 arithmetic, cross-CTA sum in fp32 pairs", "data": "synthetic",
         "config": {"workload": (f"loss64k: the 64k pack's {lay.K} episodes (latent F = {lay.seg_frames[0].tolist()}) "
                                 f"on the latent grid, {LOSS_GRID} positions x {C} channels per frame, "
                                 f"{frames} frames of capacity (L = {L}, {n_valid} valid positions)"),

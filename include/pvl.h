@@ -325,8 +325,8 @@ PVL_API pvl_status adaln_bwd(const pvl_bf16* x, const float* scale, const pvl_bf
  * a loss that is the objective: grad_scale = its weight).
  * masked_mse_loss_bwd writes only the gradient, scaled by the device value
  * dloss[0] (the autograd form).  Padding tokens' pred and target are never
- * read.  One cooperative launch (its CTAs meet at a bounded grid barrier
- * once the valid tokens are counted).  ws: dev scratch of
+ * read.  One cooperative launch (with the gradient, its CTAs meet at a
+ * bounded grid barrier once the valid tokens are counted).  ws: dev scratch of
  * masked_mse_ws_bytes(B, L, C) bytes, contents on entry ignored, one per
  * call in flight.  The loss is deterministic for a
  * given GPU model (fixed grid, fixed summation order).  pred, target,

@@ -17,17 +17,21 @@
 // so the CTAs may wait on one another), after a 64-byte clear of the
 // workspace counters:
 //   - each CTA counts the valid tokens of its share of seq_id while its
-//     first block of data is in flight, adds the count to one 64-bit total
-//     (integer atomics: exact in any order) and arrives at a grid barrier (a
-//     bounded wait: on expiry the kernel records a timeout and returns);
-//   - after the barrier every CTA reads n_valid once, then streams its
-//     grid-stride share of 16-byte vectors: the token's id decides whether
-//     pred and target are read at all (padding tokens cost no reads), the
-//     squared error goes into a per-thread fp32 sum and the gradient is
-//     written in the same pass, the next block's ids fetched while the
-//     current block's data is in flight;
-//   - CTA sums land in fp64 slots; the last CTA to finish adds them in CTA
-//     order, so the loss is deterministic for a given grid.
+//     first block of data is in flight and adds (one arrival | its count) to
+//     one 64-bit word in one integer atomic (exact in any order);
+//   - with the gradient, a grid barrier on that word (a bounded wait: on
+//     expiry the kernel records a timeout and returns): a CTA that sees every
+//     arrival in the word sees the whole count too, so no fence is needed.
+//     The loss alone needs no barrier;
+//   - every CTA streams its grid-stride share of 16-byte vectors: the
+//     token's id decides whether pred and target are read at all (padding
+//     tokens cost no reads), the squared error goes into a per-thread fp32
+//     sum and the gradient is written in the same pass, the next block's ids
+//     fetched while the current block's data is in flight;
+//   - the CTA's sum (its warps' fp32 sums added as a pair hi + lo of fp32
+//     values) lands in a slot; the last CTA to finish adds the slots in CTA
+//     order, also as a pair, and divides once: the loss is deterministic for
+//     a given grid, and no step uses the fp64 unit, which this GPU has few of.
 #include <cuda_runtime.h>
 
 #include "pvl_device.cuh"
@@ -41,11 +45,10 @@ constexpr int kUnroll = 4;
 constexpr uint32_t kSiteGridBarrier = 61;
 
 // workspace layout (bytes); the first 64 are cleared before every launch
-constexpr size_t kWsArrive = 0;                              // uint32 grid-barrier arrivals
-constexpr size_t kWsDone = 4;                                // uint32 CTAs finished
-constexpr size_t kWsTotal = 8;                               // uint64 valid tokens (integer sum: exact)
+constexpr size_t kWsCount = 0;   // uint64: CTAs arrived (high 32 bits) | valid tokens counted (low 32 bits)
+constexpr size_t kWsDone = 8;    // uint32: CTAs finished
 constexpr size_t kWsClear = 64;
-constexpr size_t kWsParts = 64;                              // double [kMaxLossCtas]
+constexpr size_t kWsParts = 64;  // per CTA its squared-error sum as a pair (hi, lo) of fp32 values
 constexpr size_t kWsBytes = kWsParts + 8 * kMaxLossCtas;
 
 struct LossParams {
@@ -73,10 +76,41 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// (hi, lo) += (bh, bl) for unevaluated pairs hi + lo of fp32 values: the
+// exact error of hi + bh (Knuth's two-sum) plus the low parts, renormalised
+// (Dekker's fast two-sum).  Commutative, so both lanes of a butterfly step
+// get the same pair.
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float bh, float bl) {
+  const float s = __fadd_rn(hi, bh);
+  const float bb = __fsub_rn(s, hi);
+  const float e = __fadd_rn(__fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(bh, bb)), __fadd_rn(lo, bl));
+  hi = __fadd_rn(s, e);
+  lo = __fsub_rn(e, __fsub_rn(hi, s));
+}
+
+// (hi + lo) / den for an integer den < 2^53: den split into dh + dl (dl
+// exact), the quotient hi / dh corrected by its remainder, which the fused
+// multiply-add gives exactly; within about one fp32 ulp.
+__device__ __forceinline__ float pair_div(float hi, float lo, unsigned long long den) {
+  const float dh = static_cast<float>(den);
+  const float dl = static_cast<float>(static_cast<long long>(den) - static_cast<long long>(dh));
+  const float q0 = __fdiv_rn(hi, dh);
+  const float r = __fadd_rn(__fsub_rn(fmaf(-q0, dh, hi), __fmul_rn(q0, dl)), lo);
+  return __fadd_rn(q0, __fdiv_rn(r, dh));
 }
 
 __device__ __forceinline__ void st_stream(void* p, uint4 v) {
@@ -88,9 +122,8 @@ template <bool kLoss, bool kGrad>
 __global__ void __launch_bounds__(kLossThreads, 2) loss_kernel(const LossParams p) {
   __shared__ uint32_t warp_n[kLossThreads / 32];
   __shared__ float warp_s[kLossThreads / 32];
-  __shared__ double warp_d[kLossThreads / 32];
   __shared__ int flag_s;
-  __shared__ unsigned long long n_valid_s;
+  __shared__ uint32_t n_valid_s;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
 
   // This thread's vectors: v0, v0 + stride, ..., taken kUnroll at a time;
@@ -133,7 +166,7 @@ __global__ void __launch_bounds__(kLossThreads, 2) loss_kernel(const LossParams 
   load_data(v0, ids, a, b);  // the first block is in flight across the count and the barrier
 
   // Valid tokens of this CTA's share of the ids (16 bytes at a time; CTA 0
-  // takes the ragged tail), added to the total, then the grid barrier.
+  // takes the ragged tail).
   {
     uint32_t n = 0;
     const long long n4 = p.n_ids / 4;
@@ -146,38 +179,46 @@ __global__ void __launch_bounds__(kLossThreads, 2) loss_kernel(const LossParams 
     if (lane == 0) warp_n[w] = n;
   }
   __syncthreads();
+  // Arrival and count go into one word in one atomic: a CTA that sees every
+  // arrival in it sees the whole count too, with no fence.
+  uint64_t* count_word = reinterpret_cast<uint64_t*>(p.ws + kWsCount);
   if (t == 0) {
-    uint32_t s = 0;
-    for (int i = 0; i < kLossThreads / 32; ++i) s += warp_n[i];
-    atomicAdd(reinterpret_cast<unsigned long long*>(p.ws + kWsTotal), static_cast<unsigned long long>(s));
-    __threadfence();
-    uint32_t* arrive = reinterpret_cast<uint32_t*>(p.ws + kWsArrive);
-    atomicAdd(arrive, 1u);  // after the fence: the count is in the total first
-    // every CTA is resident (cooperative launch), so the wait ends unless
-    // something is broken; it is bounded all the same
-    int ok = 1;
-    const uint64_t t0 = global_timer_ns();
-    while (ld_acquire(arrive) < gridDim.x) {
-      __nanosleep(200);
-      if (global_timer_ns() - t0 > p.timeout_ns) {
-        if (atomicCAS(&p.err->code, 0u, kDevErrTimeout) == 0u) {
-          p.err->where = kSiteGridBarrier;
-          p.err->block = blockIdx.x;
-          p.err->thread = 0;
-        }
-        ok = 0;
-        break;
-      }
-    }
-    n_valid_s = __ldcg(reinterpret_cast<const unsigned long long*>(p.ws + kWsTotal));
-    flag_s = ok;
+    uint32_t cta_n = 0;
+    for (int i = 0; i < kLossThreads / 32; ++i) cta_n += warp_n[i];
+    atomicAdd(reinterpret_cast<unsigned long long*>(count_word), (1ull << 32) | cta_n);
   }
-  __syncthreads();
-  if (!flag_s) return;
-  const unsigned long long n_valid = n_valid_s;
-  const float denom = static_cast<float>(p.C) * static_cast<float>(n_valid);
+
   float norm = 0.0f;
-  if (kGrad && n_valid > 0) norm = 2.0f * (p.dloss ? *p.dloss : p.grad_scale) / denom;
+  if constexpr (kGrad) {
+    // The gradient needs n_valid: a grid barrier on the count word.  Every
+    // CTA is resident (cooperative launch), so the wait ends unless something
+    // is broken; it is bounded all the same.
+    if (t == 0) {
+      int ok = 1;
+      const uint64_t t0 = global_timer_ns();
+      uint64_t c = ld_relaxed(count_word);
+      while ((c >> 32) < gridDim.x) {
+        __nanosleep(100);
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+          if (atomicCAS(&p.err->code, 0u, kDevErrTimeout) == 0u) {
+            p.err->where = kSiteGridBarrier;
+            p.err->block = blockIdx.x;
+            p.err->thread = 0;
+          }
+          ok = 0;
+          break;
+        }
+        c = ld_relaxed(count_word);
+      }
+      n_valid_s = static_cast<uint32_t>(c);
+      flag_s = ok;
+    }
+    __syncthreads();
+    if (!flag_s) return;
+    const uint32_t n_valid = n_valid_s;
+    if (n_valid > 0)
+      norm = 2.0f * (p.dloss ? *p.dloss : p.grad_scale) / (static_cast<float>(p.C) * static_cast<float>(n_valid));
+  }
 
   float sse = 0.0f;
   for (long long v = v0; v < p.n_vec; v += kUnroll * stride) {
@@ -203,36 +244,43 @@ __global__ void __launch_bounds__(kLossThreads, 2) loss_kernel(const LossParams 
     for (int u = 0; u < kUnroll; ++u) ids[u] = ids_next[u];
     load_data(v + kUnroll * stride, ids, a, b);
   }
+
   if constexpr (kLoss) {
-    // CTA sum (fp32 inside the CTA, fp64 across CTAs), then the last CTA adds
-    // the CTA sums in CTA order.
+    // The CTA's sum (fp32 inside each warp, then the warp sums as a pair
+    // hi + lo of fp32 values, about 48 significant bits) goes to its slot;
+    // the last CTA to finish adds the slots in a fixed order, so the loss is
+    // deterministic for a given grid, and needs no fp64 unit.  Every CTA added
+    // its count before it counted itself done (release), so the last one
+    // (acquire) reads the whole count.
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sse += __shfl_xor_sync(0xffffffffu, sse, o);
     if (lane == 0) warp_s[w] = sse;
     __syncthreads();
-    double* parts = reinterpret_cast<double*>(p.ws + kWsParts);
-    if (t == 0) {
-      double s = 0.0;
-      for (int i = 0; i < kLossThreads / 32; ++i) s += warp_s[i];
-      parts[blockIdx.x] = s;
-      __threadfence();
-      const uint32_t done = atomicAdd(reinterpret_cast<uint32_t*>(p.ws + kWsDone), 1u);
-      flag_s = done == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!flag_s) return;
-    __threadfence();
-    double s = 0.0;
-    for (int i = t; i < static_cast<int>(gridDim.x); i += kLossThreads) s += __ldcg(parts + i);
+    if (w != 0) return;
+    float hi = lane < kLossThreads / 32 ? warp_s[lane] : 0.0f, lo = 0.0f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) warp_d[w] = s;
-    __syncthreads();
-    if (t == 0) {
-      double total = 0.0;
-      for (int i = 0; i < kLossThreads / 32; ++i) total += warp_d[i];
-      *p.loss = n_valid > 0 ? static_cast<float>(total / (static_cast<double>(p.C) * static_cast<double>(n_valid)))
-                            : 0.0f;
+    for (int o = 16; o > 0; o >>= 1)
+      pair_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, o), __shfl_xor_sync(0xffffffffu, lo, o));
+    float2* parts = reinterpret_cast<float2*>(p.ws + kWsParts);
+    uint32_t last = 0;
+    if (lane == 0) {
+      parts[blockIdx.x] = make_float2(hi, lo);
+      last = atom_add_acq_rel(reinterpret_cast<uint32_t*>(p.ws + kWsDone), 1u) == gridDim.x - 1;
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __syncwarp();     // the other lanes read after lane 0's acquire
+    fence_acq_rel();
+    hi = lo = 0.0f;
+    for (int i = lane; i < static_cast<int>(gridDim.x); i += 32) {
+      const float2 q = __ldcg(parts + i);
+      pair_add(hi, lo, q.x, q.y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      pair_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, o), __shfl_xor_sync(0xffffffffu, lo, o));
+    if (lane == 0) {
+      const uint32_t n_valid = static_cast<uint32_t>(ld_relaxed(count_word));
+      *p.loss = n_valid > 0 ? pair_div(hi, lo, static_cast<unsigned long long>(p.C) * n_valid) : 0.0f;
     }
   }
 }
@@ -277,11 +325,11 @@ pvl_status launch(LossParams p, int B, int L, int C, size_t ws_bytes, cudaStream
   p.vec_per_tok = C / 8;
   p.n_vec = p.n_ids * (C / 8);
   p.timeout_ns = kDefaultTimeoutNs;
-  pvl_status st = check_cuda(cudaMemsetAsync(p.ws, 0, kWsClear, s), who);
-  if (st != PVL_OK) return st;
   long long needed = (p.n_vec + static_cast<long long>(kLossThreads) * kUnroll - 1) /
                      (static_cast<long long>(kLossThreads) * kUnroll);
   if (needed < 1) needed = 1;
+  const pvl_status st = check_cuda(cudaMemsetAsync(p.ws, 0, kWsClear, s), who);
+  if (st != PVL_OK) return st;
   if (p.loss && p.grad) return launch_loss<true, true>(p, needed, sms, s, who);
   if (p.loss) return launch_loss<true, false>(p, needed, sms, s, who);
   return launch_loss<false, true>(p, needed, sms, s, who);

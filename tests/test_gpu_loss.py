@@ -6,10 +6,11 @@ valid_frames[b]) on pad-collated rows and from the oracle's own seq_ids on
 concatenated rows; the kernels take the seq_ids the library builds.
 
 Tolerances, from the arithmetic: the loss is a sum of fp32 squares of exact
-bf16 differences, fp32 inside a CTA and fp64 across CTAs, so its relative
-error is ~1e-6; the test allows 1e-5.  The gradient is rounded once to bf16
-(2^-9 relative): per element |err| <= 2^-8 |ref| + 1e-30, exact zeros on
-padding tokens.
+bf16 differences, added in fp32 inside a warp and as pairs of fp32 values
+(about 48 significant bits) across warps and CTAs, so its relative error is
+~1e-6; the test allows 1e-5.  The gradient is rounded once to bf16 (2^-9
+relative): per element |err| <= 2^-8 |ref| + 1e-30, exact zeros on padding
+tokens.
 """
 
 import numpy as np
