@@ -102,9 +102,10 @@ __device__ __forceinline__ void pair_add(float& hi, float& lo, float bh, float b
   lo = __fsub_rn(e, __fsub_rn(hi, s));
 }
 
-// (hi + lo) / den for an integer den < 2^53: den split into dh + dl (dl
-// exact), the quotient hi / dh corrected by its remainder, which the fused
-// multiply-add gives exactly; within about one fp32 ulp.
+// (hi + lo) / den for an integer den < 2^48 (here C n_valid < 2^40): den
+// split into dh + dl (dl exact), the quotient hi / dh corrected by its
+// remainder, which the fused multiply-add gives exactly; within about one
+// fp32 ulp.
 __device__ __forceinline__ float pair_div(float hi, float lo, unsigned long long den) {
   const float dh = static_cast<float>(den);
   const float dl = static_cast<float>(static_cast<long long>(den) - static_cast<long long>(dh));
