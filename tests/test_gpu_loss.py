@@ -82,7 +82,15 @@ def test_concat64k_latent_grid(pvl):
     capacity."""
     lay = wl.config_layout(4)
     frames = lay.L // lay.tokens_per_frame
-    run_case(pvl, lay.seg_frames, lay.seg_valid, 128, frames * 128, 48, seed=4004)
+    pred, target, sid, loss, grad, _ = run_case(pvl, lay.seg_frames, lay.seg_valid, 128, frames * 128, 48,
+                                                seed=4004)
+    # the loss alone (no grid barrier: the last CTA reads the count) and the
+    # gradient alone give the same bits as the fused call, over a full grid
+    loss_only = pvl.masked_mse_loss(pred, target, sid)
+    grad_only = pvl.masked_mse_loss_bwd(pred, target, sid, torch.ones(1, device="cuda"))
+    pvl.device_error()
+    assert torch.equal(loss_only, loss)
+    assert torch.equal(grad_only, grad)
 
 
 def test_random_layouts(pvl):
