@@ -41,7 +41,7 @@ namespace {
 
 constexpr int kLossThreads = 512;
 constexpr int kMaxLossCtas = 2048;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 2;
 constexpr uint32_t kSiteGridBarrier = 61;
 
 // workspace layout (bytes); the first 64 are cleared before every launch
