@@ -31,7 +31,8 @@
 //   - the CTA's sum (its warps' fp32 sums added as a pair hi + lo of fp32
 //     values) lands in a slot; the last CTA to finish adds the slots in CTA
 //     order, also as a pair, and divides once: the loss is deterministic for
-//     a given grid, and no step uses the fp64 unit, which this GPU has few of.
+//     a given grid, and no step uses fp64, which GB300 runs at a small
+//     fraction of its fp32 rate.
 #include <cuda_runtime.h>
 
 #include "pvl_device.cuh"
