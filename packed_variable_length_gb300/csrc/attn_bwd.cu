@@ -244,28 +244,37 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restric
 // P^T and dS^T for the 64 query columns of group g of one key row: reads
 // S^T and dP^T from TMEM, LSE*log2e / Delta / seq_id from shared memory,
 // writes P^T (packed bf16) back over S^T columns this group has read and
-// dS^T (bf16) into the swizzled shared tile.  kMasked: PARTIAL tile.
+// dS^T (bf16) into the swizzled shared tile.  kMasked: PARTIAL tile.  Four
+// chunks of 16 queries: the next chunk's S^T and dP^T are read from TMEM
+// while the current one is computed (1.8 % off the main kernel against two
+// chunks of 32 read one after the other).
 template <bool kMasked>
 __device__ __forceinline__ void pds_chunks(uint32_t tmem_lane, int g, int row, uint32_t sDST, const float* lse2_s,
                                            const float* delta_s, const int32_t* qseq_s, int my_seq, float scale_log2) {
   const float2 c2 = make_float2(scale_log2, scale_log2);
-#pragma unroll 1
-  for (int c2i = 0; c2i < 2; ++c2i) {
-    uint32_t rs[32], rd[32];
-    tmem_ld32(tmem_lane + kColS + 64 * g + 32 * c2i, rs);
-    tmem_ld32(tmem_lane + kColDP + 64 * g + 32 * c2i, rd);
-    tmem_wait_ld();
-    uint32_t pp[16], dd[16];
+  uint32_t rs[2][16], rd[2][16];
+  tmem_ld16(tmem_lane + kColS + 64 * g, rs[0]);
+  tmem_ld16(tmem_lane + kColDP + 64 * g, rd[0]);
 #pragma unroll
-    for (int e4 = 0; e4 < 32; e4 += 4) {
-      const int q = 64 * g + 32 * c2i + e4;
+  for (int c = 0; c < 4; ++c) {
+    const int cur = c & 1;
+    tmem_wait_ld_regs(rs[cur], rd[cur]);
+    if (c + 1 < 4) {
+      tmem_ld16(tmem_lane + kColS + 64 * g + 16 * (c + 1), rs[cur ^ 1]);
+      tmem_ld16(tmem_lane + kColDP + 64 * g + 16 * (c + 1), rd[cur ^ 1]);
+    }
+    uint32_t pp[8], dd[8];
+#pragma unroll
+    for (int e4 = 0; e4 < 16; e4 += 4) {
+      const int q = 64 * g + 16 * c + e4;
       const float4 l4 = *reinterpret_cast<const float4*>(lse2_s + q);
       const float4 d4 = *reinterpret_cast<const float4*>(delta_s + q);
 #pragma unroll
       for (int u = 0; u < 4; u += 2) {
         const float2 lv = u == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w);
         const float2 dv = u == 0 ? make_float2(-d4.x, -d4.y) : make_float2(-d4.z, -d4.w);
-        const float2 x = ffma2(make_float2(__uint_as_float(rs[e4 + u]), __uint_as_float(rs[e4 + u + 1])), c2, lv);
+        const float2 x = ffma2(make_float2(__uint_as_float(rs[cur][e4 + u]), __uint_as_float(rs[cur][e4 + u + 1])),
+                               c2, lv);
         float2 pv = make_float2(ex2(x.x), ex2(x.y));
         if (kMasked) {
           const int4 s4 = *reinterpret_cast<const int4*>(qseq_s + q);
@@ -273,15 +282,19 @@ __device__ __forceinline__ void pds_chunks(uint32_t tmem_lane, int g, int row, u
           if (my_seq < 0 || sa != my_seq) pv.x = 0.0f;
           if (my_seq < 0 || sb != my_seq) pv.y = 0.0f;
         }
-        const float2 ds = fmul2(pv, fadd2(make_float2(__uint_as_float(rd[e4 + u]), __uint_as_float(rd[e4 + u + 1])), dv));
+        const float2 ds =
+            fmul2(pv, fadd2(make_float2(__uint_as_float(rd[cur][e4 + u]), __uint_as_float(rd[cur][e4 + u + 1])), dv));
         pp[(e4 + u) / 2] = pack_bf16x2(pv.x, pv.y);
         dd[(e4 + u) / 2] = pack_bf16x2(ds.x, ds.y);
       }
     }
-    tmem_st16(tmem_lane + kColS + 64 * g + 16 * c2i, pp);
+    // packed P^T of these 16 queries goes to columns [8 c, 8 c + 8) of the
+    // group's S^T, whose values chunk c / 2 <= c has already read (the load
+    // in flight reads columns 16 (c + 1) and up)
+    tmem_st8(tmem_lane + kColS + 64 * g + 8 * c, pp);
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const uint32_t off = static_cast<uint32_t>(g) * 16384 + sw128_offset(row, c2i * 4 + v);
+    for (int v = 0; v < 2; ++v) {
+      const uint32_t off = static_cast<uint32_t>(g) * 16384 + sw128_offset(row, c * 2 + v);
       st_shared_v4(sDST + off, dd[4 * v], dd[4 * v + 1], dd[4 * v + 2], dd[4 * v + 3]);
     }
   }
