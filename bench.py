@@ -1034,13 +1034,14 @@ def run_loss(args):
                 "note": "per step: pred and target copied in, seq_ids built from the host segment table, the "
                         "loss call, the loss read back; neighbouring steps' copies overlap the compute (two buffer "
                         "sets, three streams)"},
-        "gpu_launches": 2 * args.steps,
-        "roofline": {"kernel": "masked_mse_loss (count + loss kernels, timed together)", "bound": "hbm",
+        "gpu_launches": args.steps,
+        "roofline": {"kernel": "masked_mse_loss (the 64-byte workspace clear and the loss kernel, timed together)",
+                     "bound": "hbm",
                      "achieved": round(bytes_step / (ms_step * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(bytes_step / (ms_step * 1e-3) / 1e9 / hbm, 4),
                      "traffic": traffic_record("masked_loss.cu", "loss64k"),
                      "peak_note": f"of {peaks['source']} (STREAM-style copy)",
-                     "algorithmic": "4 C per valid position + 2 C per position + 4 per id, bytes per launch pair"},
+                     "algorithmic": "4 C per valid position + 2 C per position + 4 per id, bytes per call"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
